@@ -1,0 +1,121 @@
+"""Planted mistakes in a copy of the oracle must be caught by the pins.
+
+Each mutant is the oracle's C source with one plausible slip (a dropped term,
+a flipped sign, a transposed operand, a wrong exponent bias, truncating ties,
+...) compiled into a temporary library.  The pin checks below (the same
+external facts test_oracle.py uses: torch/numpy casts, closed forms, exact
+rational sums) are run against it; at least one must fail.  The real oracle
+must pass all of them.  CPU only; the mutants never touch a GPU.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_gemv_02_gb300 import inputs
+
+MUTANTS = {
+    "dropped_last_term": ("for (int64_t j = 0; j < k; ++j) {", "for (int64_t j = 0; j + 1 < k; ++j) {"),
+    "dropped_first_term": ("for (int64_t j = 0; j < k; ++j) {", "for (int64_t j = 1; j < k; ++j) {"),
+    "sign_flip": ("      acc += p;", "      acc -= p;"),
+    "transposed_B": ("B[i * k + j]", "B[i + j * n]"),
+    "reversed_a": ("* ref_decode_bits(a[j], in_fmt)", "* ref_decode_bits(a[k - 1 - j], in_fmt)"),
+    "row_stride": ("B[i * k + j]", "B[i * (k - (k > 1)) + j]"),
+    "bias_off_by_one": ("const int bias = (1 << (ebits - 1)) - 1;\n  const uint32_t emax_field = (1u << ebits) - 1u;\n  const uint32_t sign = (bits",
+                        "const int bias = (1 << (ebits - 1));\n  const uint32_t emax_field = (1u << ebits) - 1u;\n  const uint32_t sign = (bits"),
+    "subnormal_scale": ("v = ldexp((double)m, 1 - bias - mbits);", "v = ldexp((double)m, -bias - mbits);"),
+    "ties_truncate": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl;"),
+    "ties_away": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
+    "abs_sum_signed": ("acc_abs += fabs(p);", "acc_abs += p;"),
+    "bf16_as_f16": ("if (fmt == REF_F16) {", "if (fmt == REF_F16 || fmt == REF_BF16) {"),
+}
+
+
+def _check_decode(o):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for fmt, tdt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        ours = o.decode(bits, fmt)
+        theirs = torch.from_numpy(bits.view(np.int16).copy()).view(tdt).double().numpy()
+        m = ~np.isnan(theirs)
+        assert (ours[m] == theirs[m]).all()
+
+
+def _check_encode(o):
+    rng = np.random.default_rng(1)
+    x = np.exp2(rng.uniform(-30, 17, 20000)) * np.where(rng.random(20000) < 0.5, -1, 1)
+    with np.errstate(over="ignore"):
+        assert (o.encode(x, "f16") == x.astype(np.float16).view(np.uint16)).all()
+    bits = np.arange(0, 0x7BFF, dtype=np.uint16)
+    mid = (bits.view(np.float16).astype(np.float64) + (bits + 1).view(np.float16).astype(np.float64)) / 2
+    assert (o.encode(mid, "f16") == np.where(bits % 2 == 0, bits, bits + 1)).all()
+
+
+def _check_closed_forms(o):
+    for fmt in ("f16", "bf16"):
+        one = inputs.to_bits(torch.ones(1, dtype=inputs.TORCH_DTYPE[fmt]))[0]
+        for n, k in ((3, 8), (5, 77)):
+            c, s = o.gemv_ref(np.full((n, k), one, np.uint16), np.full(k, one, np.uint16), fmt)
+            assert c.tolist() == [float(k)] * n and s.tolist() == [float(k)] * n
+        for n, k in ((6, 10), (10, 6)):
+            rng = np.random.default_rng(n + k)
+            B = np.zeros((n, k), np.uint16)
+            for i in range(min(n, k)):
+                B[i, i] = one
+            a = inputs.to_bits(torch.from_numpy(rng.uniform(-2, 2, k).astype(np.float32))
+                               .to(inputs.TORCH_DTYPE[fmt]))
+            c, _ = o.gemv_ref(B, a, fmt)
+            expect = np.zeros(n)
+            expect[: min(n, k)] = inputs.from_bits(a, fmt).double().numpy()[: min(n, k)]
+            assert (c == expect).all()
+
+
+def _check_bruteforce(o):
+    for fmt in ("f16", "bf16"):
+        for seed in range(3):
+            rng = np.random.default_rng(seed)
+            tdt = inputs.TORCH_DTYPE[fmt]
+            B = inputs.to_bits(torch.from_numpy(rng.uniform(-2, 2, (4, 8)).astype(np.float32)).to(tdt))
+            a = inputs.to_bits(torch.from_numpy(rng.uniform(-2, 2, 8).astype(np.float32)).to(tdt))
+            Bv = inputs.from_bits(B, fmt).double().numpy()
+            av = inputs.from_bits(a, fmt).double().numpy()
+            c, s = o.gemv_ref(B, a, fmt)
+            for i in range(4):
+                terms = [Fraction(float(Bv[i, j])) * Fraction(float(av[j])) for j in range(8)]
+                S = sum(abs(t) for t in terms)
+                assert abs(Fraction(c[i]) - sum(terms)) <= Fraction(7, 2 ** 53) * S
+                assert abs(Fraction(s[i]) - S) <= Fraction(7, 2 ** 53) * S
+
+
+PINS = [_check_decode, _check_encode, _check_closed_forms, _check_bruteforce]
+
+
+def _failures(o):
+    failed = []
+    for pin in PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_real_oracle_passes_every_pin():
+    assert _failures(oracle.default()) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    lib = oracle.build(force=True, src=str(path), out=str(tmp_path / "libmutant.so"))
+    failed = _failures(oracle.Oracle(lib))
+    assert failed, f"mutant {name} passed every pin"
