@@ -1,0 +1,205 @@
+/*
+ * gemv.h -- C ABI of the GB300 (sm_103a) matrix-vector product library.
+ *
+ * The operation (TileLang Case Studies, Case B "Background"): B is an (n, k)
+ * matrix stored row-major with leading dimension k, a is a (k,) vector, and
+ *
+ *     c[i] = sum_{j < k} B[i, j] * a[j]        for i < n.
+ *
+ * B and a are both IEEE binary16 (fp16) or both bfloat16.  Products and sums
+ * are formed in fp32; the result is rounded once (nearest-even) to the output
+ * type, which is the input type or fp32.  The summation order is not part of
+ * the contract (it is fixed for a given shape, dtype and launch
+ * configuration, so repeated calls are bitwise reproducible).
+ *
+ * Conventions shared by every entry point:
+ *  - Device pointers are plain CUDA device addresses on the CURRENT device
+ *    (cudaGetDevice at the time of the call).  The caller owns B, a and c; the
+ *    library never frees or retains them past the call.
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream); the
+ *    caller synchronizes before reading c.
+ *  - Nothing throws across this boundary and nothing calls exit/abort: every
+ *    failure is a negative status code (GEMV_ERR_*), and on failure nothing
+ *    has been launched.  gemv_status_string() describes a code.
+ *  - Thread-safe: the launch-configuration cache and workspace table are
+ *    guarded internally.  Per-thread state: gemv_last_config, the last CUDA
+ *    error code.
+ */
+#ifndef GEMV_GB300_H_
+#define GEMV_GB300_H_
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes: input type of B and a, and output type of c. */
+enum {
+  GEMV_F16 = 0,          /* fp16 B, a -> fp16 c */
+  GEMV_BF16 = 1,         /* bf16 B, a -> bf16 c */
+  GEMV_F16_OUT_F32 = 2,  /* fp16 B, a -> fp32 c */
+  GEMV_BF16_OUT_F32 = 3  /* bf16 B, a -> fp32 c */
+};
+
+/* Status codes. */
+enum {
+  GEMV_OK = 0,
+  GEMV_ERR_ARG = -1,     /* null pointer with n > 0 and k > 0, n < 0, k < 0, k > INT32_MAX */
+  GEMV_ERR_DTYPE = -2,   /* unknown dtype code */
+  GEMV_ERR_ALIAS = -3,   /* c overlaps B or a */
+  GEMV_ERR_DEVICE = -4,  /* no CUDA device, or the current device is not sm_103 */
+  GEMV_ERR_CUDA = -5,    /* a CUDA call or launch failed; see gemv_last_cuda_error() */
+  GEMV_ERR_CONFIG = -6,  /* a forced configuration is invalid for this shape */
+  GEMV_ERR_ALIGN = -7,   /* B or a not 2-byte aligned, or c not aligned to its element */
+  GEMV_ERR_NOMEM = -8    /* the split-K workspace could not be allocated */
+};
+
+/* Kernel variants (gemv_config.variant). */
+enum {
+  GEMV_VARIANT_AUTO = 0,         /* let the planner choose */
+  GEMV_VARIANT_ROWS = 1,         /* rows stream as aligned 16-byte vectors; needs k % 8 == 0
+                                    and B 16-byte aligned */
+  GEMV_VARIANT_ROWS_GENERAL = 2  /* any k and any 2-byte-aligned B: each row is read as the
+                                    aligned 16-byte blocks covering it, edge elements masked,
+                                    and a is realigned in registers by the row's offset */
+};
+
+/*
+ * A launch configuration.  As input to gemv_ex()/gemv_plan(), a zero field
+ * means "planner's choice".  As output, every field is filled in.
+ *
+ *  variant        GEMV_VARIANT_*.
+ *  rows_per_warp  R: rows one warp streams side by side (1, 2 or 4; 1 for
+ *                 the general variant).  The a-vector chunk read from shared
+ *                 memory is reused across the R rows.
+ *  warps_per_cta  W: 4, 8 or 16 warps per CTA.
+ *  warp_split     Sw: warps of one CTA that share a row, each streaming a
+ *                 contiguous slice of it; their partial sums are combined
+ *                 in shared memory in a fixed order.  Divides W.
+ *  grid_split     Sg: CTAs that share a block of rows, each over one k-segment.
+ *                 Sg > 1 writes fp32 partials to a workspace and launches a
+ *                 second kernel that adds them in segment order (split-K).
+ *  ctas           total CTAs of the main kernel (row blocks x Sg).
+ *  smem_bytes     dynamic shared memory per CTA (the staged a segment plus
+ *                 the cross-warp partials).
+ *  launches       kernels per call: 1, or 2 with split-K.
+ *  k_segment      columns per k-segment (a multiple of 8 except when Sg == 1).
+ *  row_blocks     number of row blocks (ctas / grid_split).
+ *  unroll         U: 16-byte loads per lane issued back to back per row.
+ */
+typedef struct gemv_config {
+  int32_t variant;
+  int32_t rows_per_warp;
+  int32_t warps_per_cta;
+  int32_t warp_split;
+  int32_t grid_split;
+  int32_t ctas;
+  int32_t smem_bytes;
+  int32_t launches;
+  int64_t k_segment;
+  int32_t row_blocks;
+  int32_t unroll;
+  int32_t reserved[4];
+} gemv_config;
+
+/*
+ * c = B @ a on the current device, asynchronously on `stream`.
+ *
+ *  B      device pointer, n*k elements, row-major (row i starts at B + i*k).
+ *         Must be 2-byte aligned; 16-byte alignment plus k % 8 == 0 selects
+ *         the aligned-vector variant, anything else the general variant.
+ *  a      device pointer, k elements, 2-byte aligned.
+ *  c      device pointer, n elements of the output type, aligned to it; must
+ *         not overlap B or a (GEMV_ERR_ALIAS).
+ *  n, k   sizes: n >= 0, 0 <= k <= INT32_MAX.  n == 0 launches nothing and
+ *         returns GEMV_OK.  k == 0 sets c to +0 (the empty sum).
+ *  dtype  GEMV_F16, GEMV_BF16, GEMV_F16_OUT_F32 or GEMV_BF16_OUT_F32.
+ *
+ * The first call for a (device, n, k, dtype, alignment) key builds and caches
+ * the launch configuration; later calls are a lookup plus one launch (two
+ * with split-K).  A split-K configuration uses a library-owned fp32
+ * workspace of grid_split*n floats per (device, stream), allocated on first
+ * need (cudaMalloc, which synchronizes the device) and kept, grow-only,
+ * until gemv_release().  Use gemv_prepare() to do that before timing or
+ * before capturing the stream in a CUDA graph.
+ */
+int gemv(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
+         cudaStream_t stream);
+
+/*
+ * As gemv(), with a configuration forced field by field (zero fields left
+ * to the planner).  `forced` may be NULL (same as gemv()).  An impossible
+ * configuration (e.g. the aligned variant for k % 8 != 0, W not in
+ * {4, 8, 16}, Sw not dividing W) returns GEMV_ERR_CONFIG.  Forced
+ * configurations are not cached.  For tests and benchmarks.
+ */
+int gemv_ex(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
+            const gemv_config *forced, cudaStream_t stream);
+
+/*
+ * Build and cache the configuration gemv() would use for (n, k, dtype) on
+ * the current device, for B with the given alignment (b_aligned16 != 0:
+ * 16-byte aligned), and reserve the split-K workspace for `stream` if the
+ * configuration needs one.  Optional; gemv() does the same lazily.
+ */
+int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cudaStream_t stream);
+
+/*
+ * The planner as a pure host function (no CUDA call): the configuration
+ * chosen for (n, k, dtype) on a device with `sm_count` SMs, for B with the
+ * given alignment class, with `forced` fields (may be NULL) honoured.
+ * Writes *out and returns GEMV_OK, or an error code.
+ */
+int gemv_plan(int64_t n, int64_t k, int dtype, int b_aligned16, int sm_count,
+              const gemv_config *forced, gemv_config *out);
+
+/* The configuration of this thread's last successful gemv/gemv_ex launch. */
+int gemv_last_config(gemv_config *out);
+
+/* Static description of a status code (never NULL). */
+const char *gemv_status_string(int status);
+
+/* The cudaError_t value behind this thread's last GEMV_ERR_CUDA (0 if none). */
+int gemv_last_cuda_error(void);
+
+/*
+ * Test hook: the next gemv/gemv_ex/gemv_host call on any thread returns
+ * `status` without launching anything (0 clears it).  Host-side only; no
+ * GPU fault is ever involved.
+ */
+int gemv_debug_inject(int status);
+
+/*
+ * Free the library-owned workspaces and drop the configuration cache.  The
+ * caller must make sure no call that uses them is still running on the GPU.
+ */
+int gemv_release(void);
+
+/*
+ * End-to-end call for a matrix and vector held in host memory: copies B
+ * (n*k elements) and a (k elements) from host to the caller's device buffers
+ * B_dev and a_dev, runs gemv() into c_dev, and copies c back to c_host, all
+ * asynchronously on `stream` (cudaMemcpyAsync; pinned host buffers make the
+ * copies truly asynchronous).  All six buffers are caller-owned.  Same
+ * status codes as gemv().
+ */
+int gemv_host(const void *B_host, const void *a_host, void *c_host, void *B_dev, void *a_dev,
+              void *c_dev, int64_t n, int64_t k, int dtype, cudaStream_t stream);
+
+/*
+ * Measurement helper, not part of the product: a read-only streaming pass
+ * over `bytes` bytes at `buf` (16-byte aligned, bytes % 16 == 0) with the
+ * same load path as the GEMV kernels, to calibrate the achievable HBM read
+ * bandwidth.  Writes one 32-bit checksum word per CTA to `sink` (device
+ * memory of at least 64 KiB).  Asynchronous on `stream`.
+ */
+int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMV_GB300_H_ */

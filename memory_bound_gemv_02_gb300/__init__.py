@@ -1,1 +1,244 @@
-"""GB300-native GEMV c = B @ a (binding added with the C-ABI library)."""
+"""GB300-native GEMV ``c = B @ a`` -- thin Python binding of the C-ABI library.
+
+B is (n, k) row-major, a is (k,), both fp16 or both bf16; products and sums in
+fp32; c in the input type or fp32 (TileLang Case Studies, Case B
+"Background").  Every step of the computation runs in the CUDA kernels of
+``_lib/libgemv.so`` (sources in ``csrc/``, ABI in ``include/gemv.h``); this
+module only marshals torch tensors into pointers, sizes and the current
+stream.  There is no CPU or PyTorch fallback: if the library has not been
+built, every call raises.
+
+Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_prepare``,
+``gemv_plan``, ``gemv_last_config``, ``gemv_status_string``,
+``gemv_last_cuda_error``, ``gemv_debug_inject``, ``gemv_release``,
+``gemv_host``, ``gemv_probe_read``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+GEMV_F16, GEMV_BF16, GEMV_F16_OUT_F32, GEMV_BF16_OUT_F32 = 0, 1, 2, 3
+GEMV_OK = 0
+GEMV_ERR_ARG, GEMV_ERR_DTYPE, GEMV_ERR_ALIAS, GEMV_ERR_DEVICE = -1, -2, -3, -4
+GEMV_ERR_CUDA, GEMV_ERR_CONFIG, GEMV_ERR_ALIGN, GEMV_ERR_NOMEM = -5, -6, -7, -8
+GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL = 0, 1, 2
+
+#: the C ABI's exported entry points (checked against include/gemv.h by the tests)
+ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_prepare", "gemv_plan", "gemv_last_config",
+                "gemv_status_string", "gemv_last_cuda_error", "gemv_debug_inject",
+                "gemv_release", "gemv_host", "gemv_probe_read")
+
+
+class GemvConfig(ctypes.Structure):
+    """Mirror of ``gemv_config`` in include/gemv.h."""
+    _fields_ = [("variant", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32), ("warp_split", ctypes.c_int32),
+                ("grid_split", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("k_segment", ctypes.c_int64), ("row_blocks", ctypes.c_int32),
+                ("unroll", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+
+    def to_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+class GemvError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        msg = gemv_status_string(status)
+        if status == GEMV_ERR_CUDA:
+            msg += f" (cudaError {gemv_last_cuda_error()})"
+        super().__init__(f"{where}: status {status}: {msg}" if where else f"status {status}: {msg}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = _build.lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"the GEMV CUDA library is not built ({path} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` -- there is no fallback")
+            L = ctypes.CDLL(path)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            cfgp = ctypes.POINTER(GemvConfig)
+            L.gemv.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+            L.gemv_ex.argtypes = [vp, vp, vp, i64, i64, i32, cfgp, vp]
+            L.gemv_prepare.argtypes = [i64, i64, i32, i32, vp]
+            L.gemv_plan.argtypes = [i64, i64, i32, i32, i32, cfgp, cfgp]
+            L.gemv_last_config.argtypes = [cfgp]
+            L.gemv_status_string.argtypes = [i32]
+            L.gemv_status_string.restype = ctypes.c_char_p
+            L.gemv_last_cuda_error.argtypes = []
+            L.gemv_debug_inject.argtypes = [i32]
+            L.gemv_release.argtypes = []
+            L.gemv_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
+            L.gemv_probe_read.argtypes = [vp, i64, vp, vp]
+            for name in ENTRY_POINTS:
+                if name != "gemv_status_string":
+                    getattr(L, name).restype = i32
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------- helpers --
+
+def dtype_code(dtype: torch.dtype, out_fp32: bool = False) -> int:
+    if dtype == torch.float16:
+        return GEMV_F16_OUT_F32 if out_fp32 else GEMV_F16
+    if dtype == torch.bfloat16:
+        return GEMV_BF16_OUT_F32 if out_fp32 else GEMV_BF16
+    raise TypeError(f"GEMV takes float16 or bfloat16 inputs, got {dtype}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _config_arg(config):
+    if config is None:
+        return None
+    if isinstance(config, GemvConfig):
+        return ctypes.byref(config)
+    c = GemvConfig()
+    for kname, v in dict(config).items():
+        setattr(c, kname, int(v))
+    return ctypes.byref(c)
+
+
+def _check(status: int, where: str):
+    if status != GEMV_OK:
+        raise GemvError(status, where)
+
+
+def _operands(B: torch.Tensor, a: torch.Tensor, c, out_fp32: bool):
+    if B.dim() != 2 or a.dim() != 1 or B.shape[1] != a.shape[0]:
+        raise ValueError(f"shape mismatch: B {tuple(B.shape)}, a {tuple(a.shape)}")
+    if B.dtype != a.dtype:
+        raise TypeError(f"B and a must share a dtype ({B.dtype} vs {a.dtype})")
+    if not (B.is_cuda and a.is_cuda):
+        raise ValueError("B and a must be CUDA tensors")
+    n, k = B.shape
+    if k > 0 and n > 0 and B.stride() != (k, 1):
+        raise ValueError("B must be row-major with leading dimension k (contiguous rows)")
+    if k > 1 and a.stride(0) != 1:
+        raise ValueError("a must be contiguous")
+    out_dtype = torch.float32 if out_fp32 else B.dtype
+    if c is None:
+        c = torch.empty(n, dtype=out_dtype, device=B.device)
+    elif c.dtype != out_dtype or c.shape != (n,) or not c.is_cuda or (n > 1 and c.stride(0) != 1):
+        raise ValueError(f"c must be a contiguous CUDA tensor of shape ({n},) and dtype {out_dtype}")
+    if B.device != a.device or B.device != c.device:
+        raise ValueError("B, a and c must be on the same device")
+    return n, k, c
+
+
+# ---------------------------------------------------------- entry points --
+
+def gemv(B: torch.Tensor, a: torch.Tensor, c: torch.Tensor | None = None, out_fp32: bool = False,
+         stream=None) -> torch.Tensor:
+    """c = B @ a on B's device, asynchronously on ``stream`` (default: the
+    current torch stream).  Returns c (allocated if not given)."""
+    n, k, c = _operands(B, a, c, out_fp32)
+    with torch.cuda.device(B.device):
+        st = lib().gemv(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
+                        dtype_code(B.dtype, out_fp32), _stream_handle(stream))
+    _check(st, "gemv")
+    return c
+
+
+def gemv_ex(B, a, c=None, out_fp32: bool = False, config=None, stream=None) -> torch.Tensor:
+    """``gemv`` with a forced launch configuration (dict or GemvConfig;
+    zero/missing fields are left to the planner)."""
+    n, k, c = _operands(B, a, c, out_fp32)
+    with torch.cuda.device(B.device):
+        st = lib().gemv_ex(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
+                           dtype_code(B.dtype, out_fp32), _config_arg(config), _stream_handle(stream))
+    _check(st, "gemv_ex")
+    return c
+
+
+def gemv_prepare(n: int, k: int, dtype: int, b_aligned16: bool = True, stream=None) -> None:
+    _check(lib().gemv_prepare(n, k, dtype, 1 if b_aligned16 else 0, _stream_handle(stream)),
+           "gemv_prepare")
+
+
+def gemv_plan(n: int, k: int, dtype: int, b_aligned16: bool, sm_count: int, config=None) -> dict:
+    """The planner's choice for a shape on a device with ``sm_count`` SMs
+    (pure host function; needs no GPU)."""
+    out = GemvConfig()
+    _check(lib().gemv_plan(n, k, dtype, 1 if b_aligned16 else 0, sm_count, _config_arg(config),
+                           ctypes.byref(out)), "gemv_plan")
+    return out.to_dict()
+
+
+def gemv_last_config() -> dict:
+    out = GemvConfig()
+    _check(lib().gemv_last_config(ctypes.byref(out)), "gemv_last_config")
+    return out.to_dict()
+
+
+def gemv_status_string(status: int) -> str:
+    return lib().gemv_status_string(int(status)).decode()
+
+
+def gemv_last_cuda_error() -> int:
+    return int(lib().gemv_last_cuda_error())
+
+
+def gemv_debug_inject(status: int) -> None:
+    lib().gemv_debug_inject(int(status))
+
+
+def gemv_release() -> None:
+    lib().gemv_release()
+
+
+def gemv_host(B_host: torch.Tensor, a_host: torch.Tensor, c_host: torch.Tensor, B_dev: torch.Tensor,
+              a_dev: torch.Tensor, c_dev: torch.Tensor, stream=None) -> torch.Tensor:
+    """End-to-end call from host buffers (pinned for true asynchrony): copies
+    B and a into the device buffers, runs the GEMV, copies c back into
+    ``c_host``.  Asynchronous on ``stream``; synchronize before reading c_host."""
+    n, k = B_host.shape
+    out_fp32 = c_host.dtype == torch.float32
+    if B_host.is_cuda or a_host.is_cuda or c_host.is_cuda:
+        raise ValueError("B_host, a_host and c_host must be host tensors")
+    if not (B_host.is_contiguous() and a_host.is_contiguous() and c_host.is_contiguous()):
+        raise ValueError("host buffers must be contiguous")
+    _operands(B_dev, a_dev, c_dev, out_fp32)
+    if B_dev.shape != B_host.shape or a_dev.shape != a_host.shape or c_dev.shape != c_host.shape:
+        raise ValueError("host and device buffers must have the same shapes")
+    with torch.cuda.device(B_dev.device):
+        st = lib().gemv_host(B_host.data_ptr(), a_host.data_ptr(), c_host.data_ptr(), B_dev.data_ptr(),
+                             a_dev.data_ptr(), c_dev.data_ptr(), n, k,
+                             dtype_code(B_host.dtype, out_fp32), _stream_handle(stream))
+    _check(st, "gemv_host")
+    return c_host
+
+
+def gemv_probe_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Read-only bandwidth probe over ``buf`` (a measurement helper)."""
+    nbytes = buf.numel() * buf.element_size()
+    if sink.numel() * sink.element_size() < 65536:
+        raise ValueError("sink must hold at least 64 KiB")
+    with torch.cuda.device(buf.device):
+        st = lib().gemv_probe_read(buf.data_ptr(), nbytes, sink.data_ptr(), _stream_handle(stream))
+    _check(st, "gemv_probe_read")

@@ -1,0 +1,538 @@
+// Host side of the GEMV library: argument checks, the launch planner, the
+// per-key configuration cache, split-K workspaces and the launches.
+//
+// The hot call (a cached key) is: validation (pure arithmetic), one
+// cudaGetDevice, one hash lookup under a mutex, and one or two kernel
+// launches.  Everything that costs more -- device attribute queries,
+// cudaFuncSetAttribute, workspace allocation -- happens once, when a key or
+// a (device, stream) pair is first seen.  This is the GB300 counterpart of
+// TileLang Case Studies Case B.4 / Case E, where per-call kernel building
+// cost 11-200 ms against a ~70 us kernel.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
+#include <unordered_map>
+#include <utility>
+
+#include "gemv.h"
+#include "gemv_internal.h"
+
+namespace gemvk {
+namespace {
+
+constexpr int64_t kMaxSegment = 32768;  // columns of a staged per CTA (64 KiB of shared memory)
+constexpr int kMaxGridSplit = 64;
+constexpr int kMaxSmemPerCta = 232448;  // 227 KiB, sm_100-family opt-in limit
+constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
+constexpr int64_t kSmemReservedPerCta = 1024;
+constexpr int kMaxDevices = 64;
+constexpr int kReduceThreads = 256;
+constexpr int kProbeSinkWords = 16384;  // 64 KiB
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+inline int64_t pow2_floor(int64_t x) {
+  int64_t p = 1;
+  while (p * 2 <= x) p *= 2;
+  return p;
+}
+inline int out_elem_bytes(int dtype) { return dtype >= 2 ? 4 : 2; }
+
+struct DeviceInfo {
+  bool init = false;
+  bool ok = false;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+};
+
+struct Key {
+  int dev;
+  int dtype;
+  int aligned;
+  int64_t n;
+  int64_t k;
+  bool operator==(const Key &o) const {
+    return dev == o.dev && dtype == o.dtype && aligned == o.aligned && n == o.n && k == o.k;
+  }
+};
+
+struct KeyHash {
+  size_t operator()(const Key &x) const {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](uint64_t v) {
+      h ^= v;
+      h *= 1099511628211ull;
+    };
+    mix((uint64_t)x.dev);
+    mix((uint64_t)x.dtype);
+    mix((uint64_t)x.aligned);
+    mix((uint64_t)x.n);
+    mix((uint64_t)x.k);
+    return (size_t)h;
+  }
+};
+
+struct Workspace {
+  float *ptr = nullptr;
+  size_t bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+std::unordered_map<Key, gemv_config, KeyHash> g_cache;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+std::set<std::pair<const void *, int>> g_func_attr_set;
+std::atomic<int> g_inject{0};
+
+thread_local gemv_config t_last{};
+thread_local bool t_has_last = false;
+thread_local int t_cuda_err = 0;
+
+int cuda_fail(cudaError_t e) {
+  t_cuda_err = (int)e;
+  return GEMV_ERR_CUDA;
+}
+
+// Device attributes, queried once per device (caller holds g_mu).
+const DeviceInfo &device_info_locked(int dev) {
+  DeviceInfo &d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+            cudaSuccess) {
+      d.ok = (major == 10 && minor == 3);
+    }
+  }
+  return d;
+}
+
+bool valid_W(int W) { return W == 4 || W == 8 || W == 16; }
+bool valid_R(int R) { return R == 1 || R == 2 || R == 4; }
+
+// The planner.  Pure host arithmetic: no CUDA call.
+int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_config *f,
+              gemv_config *out) {
+  if (dtype < 0 || dtype > 3) return GEMV_ERR_DTYPE;
+  if (n < 1 || k < 1 || k > INT32_MAX || sm < 1) return GEMV_ERR_ARG;
+  gemv_config fz{};
+  if (f == nullptr) f = &fz;
+
+  const int variant = f->variant ? f->variant : (aligned ? GEMV_VARIANT_ROWS : GEMV_VARIANT_ROWS_GENERAL);
+  if (variant != GEMV_VARIANT_ROWS && variant != GEMV_VARIANT_ROWS_GENERAL) return GEMV_ERR_CONFIG;
+  if (variant == GEMV_VARIANT_ROWS && !aligned) return GEMV_ERR_CONFIG;
+
+  const int64_t nt = cdiv(k, 8);  // 16-byte vectors per row
+  const int64_t warp_slots = (int64_t)sm * 32;  // 32 resident warps per SM
+  int R;
+  if (f->rows_per_warp) {
+    R = f->rows_per_warp;
+    if (!valid_R(R)) return GEMV_ERR_CONFIG;
+  } else if (variant == GEMV_VARIANT_ROWS_GENERAL) {
+    R = 1;
+  } else if (n >= warp_slots * 4 && k * 2 <= 2048) {
+    R = 4;
+  } else if (n >= warp_slots * 2 && k * 2 <= 8192) {
+    R = 2;
+  } else {
+    R = 1;
+  }
+  if (variant == GEMV_VARIANT_ROWS_GENERAL && R != 1) return GEMV_ERR_CONFIG;
+
+  const int64_t row_groups = cdiv(n, R);
+  // Splits of a row needed so that every warp slot of the GPU has work, and
+  // the most that still leave every lane at least two 16-byte loads.
+  const int64_t want = row_groups >= warp_slots ? 1 : cdiv(warp_slots, row_groups);
+  const int64_t max_split = nt / 64 > 1 ? nt / 64 : 1;
+  const int64_t split = want < max_split ? want : max_split;
+
+  gemv_config best{};
+  bool have = false;
+  const int W_list[3] = {16, 8, 4};
+  for (int wi = 0; wi < 3; ++wi) {
+    const int W = f->warps_per_cta ? f->warps_per_cta : W_list[wi];
+    if (!valid_W(W)) return GEMV_ERR_CONFIG;
+    int Sw;
+    if (f->warp_split) {
+      Sw = f->warp_split;
+      if (Sw < 1 || Sw > W || W % Sw != 0) return GEMV_ERR_CONFIG;
+    } else {
+      Sw = (int)(pow2_floor(split) < W ? pow2_floor(split) : W);
+    }
+    int64_t Sg;
+    if (f->grid_split) {
+      Sg = f->grid_split;
+      if (Sg < 1 || Sg > kMaxGridSplit) return GEMV_ERR_CONFIG;
+    } else {
+      Sg = cdiv(k, kMaxSegment);
+      const int64_t need = split > Sw ? cdiv(split, Sw) : 1;
+      if (need > Sg) Sg = need;
+      if (Sg > kMaxGridSplit) Sg = kMaxGridSplit;
+      // a forced CTA count caps the split (but not below what k requires)
+      if (f->ctas && Sg > f->ctas) Sg = f->ctas > cdiv(k, kMaxSegment) ? f->ctas : cdiv(k, kMaxSegment);
+    }
+    int64_t kseg = (Sg == 1) ? k : round_up(cdiv(k, Sg), 8);
+    Sg = cdiv(k, kseg);  // every segment non-empty
+    if (kseg > kMaxSegment) return GEMV_ERR_CONFIG;
+
+    // CTAs resident per SM: 32 warps by the kernel's register bound (at most
+    // 64 registers a thread), fewer if shared memory runs out first.
+    int cps = 32 / W;
+    const int64_t as_elems = round_up(kseg + 24, 8);
+    const int64_t smem = as_elems * 2 + (int64_t)W * R * 4;
+    if (smem > kMaxSmemPerCta) return GEMV_ERR_CONFIG;
+    const int64_t cps_smem = kSmemPerSm / (smem + kSmemReservedPerCta);
+    if (cps_smem < cps) cps = (int)cps_smem;
+    const int64_t slots = W / Sw;
+    const int64_t max_rb = ((int64_t)sm * cps) / Sg > 0 ? ((int64_t)sm * cps) / Sg : 1;
+    int64_t nrb;
+    if (f->ctas) {
+      if (f->ctas < Sg) return GEMV_ERR_CONFIG;
+      nrb = f->ctas / Sg;
+    } else {
+      nrb = cdiv(n, slots * R);
+      if (nrb > max_rb) nrb = max_rb;
+    }
+    if (nrb * Sg > INT32_MAX) return GEMV_ERR_CONFIG;
+
+    gemv_config c{};
+    c.variant = variant;
+    c.rows_per_warp = R;
+    c.warps_per_cta = W;
+    c.warp_split = Sw;
+    c.grid_split = (int32_t)Sg;
+    c.row_blocks = (int32_t)nrb;
+    c.ctas = (int32_t)(nrb * Sg);
+    c.smem_bytes = (int32_t)smem;
+    c.launches = Sg > 1 ? 2 : 1;
+    c.k_segment = kseg;
+    c.unroll = unroll_for_rows(R);
+    best = c;
+    have = true;
+    // Prefer big CTAs unless that leaves SMs idle; a forced W ends the search.
+    if (f->warps_per_cta || c.ctas >= sm) break;
+  }
+  if (!have) return GEMV_ERR_CONFIG;
+  *out = best;
+  return GEMV_OK;
+}
+
+MainKernel lookup_main(int dtype, const gemv_config &c) {
+  const int of = dtype >= 2 ? 1 : 0;
+  return (dtype & 1) ? main_kernel_bf16(of, c.variant, c.rows_per_warp)
+                     : main_kernel_f16(of, c.variant, c.rows_per_warp);
+}
+
+ReduceKernel lookup_reduce(int dtype) {
+  const int of = dtype >= 2 ? 1 : 0;
+  return (dtype & 1) ? reduce_kernel_bf16(of) : reduce_kernel_f16(of);
+}
+
+// Opt a kernel into more than 48 KiB of dynamic shared memory on this
+// device, once (caller holds g_mu).
+cudaError_t ensure_smem_attr_locked(const void *fn, int dev, int smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  auto key = std::make_pair(fn, dev);
+  if (g_func_attr_set.count(key)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerCta);
+  if (e == cudaSuccess) g_func_attr_set.insert(key);
+  return e;
+}
+
+// Workspace of at least `bytes` for (dev, stream) (caller holds g_mu).
+int workspace_locked(int dev, cudaStream_t stream, size_t bytes, float **out) {
+  Workspace &w = g_ws[std::make_pair(dev, stream)];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      // The previous buffer may still be in use by work queued on `stream`.
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    void *p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMV_ERR_NOMEM;
+    }
+    w.ptr = static_cast<float *>(p);
+    w.bytes = bytes;
+  }
+  *out = w.ptr;
+  return GEMV_OK;
+}
+
+bool overlaps(const void *p, int64_t pbytes, const void *q, int64_t qbytes) {
+  const uintptr_t a0 = (uintptr_t)p, a1 = a0 + (uintptr_t)pbytes;
+  const uintptr_t b0 = (uintptr_t)q, b1 = b0 + (uintptr_t)qbytes;
+  return a0 < b1 && b0 < a1;
+}
+
+// Checks that need no CUDA call.  Returns GEMV_OK or an error; sets *done
+// when nothing has to be launched (n == 0).
+int validate(const void *B, const void *a, const void *c, int64_t n, int64_t k, int dtype) {
+  if (dtype < 0 || dtype > 3) return GEMV_ERR_DTYPE;
+  if (n < 0 || k < 0 || k > INT32_MAX) return GEMV_ERR_ARG;
+  if (n == 0) return GEMV_OK;
+  if (c == nullptr) return GEMV_ERR_ARG;
+  if (k > 0 && (B == nullptr || a == nullptr)) return GEMV_ERR_ARG;
+  const int oe = out_elem_bytes(dtype);
+  if (((uintptr_t)c % (uintptr_t)oe) != 0) return GEMV_ERR_ALIGN;
+  if (k > 0 && (((uintptr_t)B & 1u) || ((uintptr_t)a & 1u))) return GEMV_ERR_ALIGN;
+  if (n > INT64_MAX / (k > 0 ? k : 1) / 2) return GEMV_ERR_ARG;
+  if (k > 0) {
+    const int64_t cb = n * oe;
+    if (overlaps(c, cb, B, n * k * 2) || overlaps(c, cb, a, k * 2)) return GEMV_ERR_ALIAS;
+  }
+  return GEMV_OK;
+}
+
+int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, const gemv_config *forced,
+        cudaStream_t stream) {
+  int inj = g_inject.exchange(0);
+  if (inj != 0) return inj;
+  int st = validate(B, a, c, n, k, dtype);
+  if (st != GEMV_OK) return st;
+  if (n == 0) return GEMV_OK;
+
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  if (k == 0) {
+    // The empty sum: +0 in every output format is all-zero bits.
+    e = cudaMemsetAsync(c, 0, (size_t)n * out_elem_bytes(dtype), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    gemv_config z{};
+    t_last = z;
+    t_has_last = true;
+    return GEMV_OK;
+  }
+  const bool aligned = (((uintptr_t)B & 15u) == 0) && (k % 8 == 0);
+
+  gemv_config cfg{};
+  float *ws = nullptr;
+  MainKernel mk = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const DeviceInfo &di = device_info_locked(dev);
+    if (!di.ok) return GEMV_ERR_DEVICE;
+    const bool is_forced = forced != nullptr && (forced->variant || forced->rows_per_warp ||
+                                                 forced->warps_per_cta || forced->warp_split ||
+                                                 forced->grid_split || forced->ctas);
+    if (is_forced) {
+      st = plan_impl(n, k, dtype, aligned, di.sm_count, forced, &cfg);
+      if (st != GEMV_OK) return st;
+    } else {
+      Key key{dev, dtype, aligned ? 1 : 0, n, k};
+      auto it = g_cache.find(key);
+      if (it != g_cache.end()) {
+        cfg = it->second;
+      } else {
+        st = plan_impl(n, k, dtype, aligned, di.sm_count, nullptr, &cfg);
+        if (st != GEMV_OK) return st;
+        g_cache.emplace(key, cfg);
+      }
+    }
+    if (cfg.smem_bytes > di.max_smem_optin) return GEMV_ERR_CONFIG;
+    mk = lookup_main(dtype, cfg);
+    if (mk == nullptr) return GEMV_ERR_CONFIG;
+    e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cfg.grid_split > 1) {
+      st = workspace_locked(dev, stream, (size_t)cfg.grid_split * (size_t)n * sizeof(float), &ws);
+      if (st != GEMV_OK) return st;
+    }
+  }
+
+  Params p;
+  p.B = static_cast<const uint16_t *>(B);
+  p.a = static_cast<const uint16_t *>(a);
+  p.c = c;
+  p.ws = ws;
+  p.n = n;
+  p.k = k;
+  p.kseg = cfg.k_segment;
+  p.base_off = (int32_t)(((uintptr_t)B >> 1) & 7u);
+  p.sg = cfg.grid_split;
+  p.sw = cfg.warp_split;
+  p.nrb = cfg.row_blocks;
+  p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
+
+  mk<<<cfg.ctas, cfg.warps_per_cta * 32, cfg.smem_bytes, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cfg.grid_split > 1) {
+    ReduceKernel rk = lookup_reduce(dtype);
+    int64_t blocks = cdiv(n, kReduceThreads);
+    if (blocks > 65535) blocks = 65535;
+    rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  t_last = cfg;
+  t_has_last = true;
+  return GEMV_OK;
+}
+
+}  // namespace
+}  // namespace gemvk
+
+using namespace gemvk;
+
+extern "C" int gemv(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
+                    cudaStream_t stream) {
+  return run(B, a, c, n, k, dtype, nullptr, stream);
+}
+
+extern "C" int gemv_ex(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
+                       const gemv_config *forced, cudaStream_t stream) {
+  return run(B, a, c, n, k, dtype, forced, stream);
+}
+
+extern "C" int gemv_plan(int64_t n, int64_t k, int dtype, int b_aligned16, int sm_count,
+                         const gemv_config *forced, gemv_config *out) {
+  if (out == nullptr) return GEMV_ERR_ARG;
+  const bool aligned = b_aligned16 != 0 && k % 8 == 0;
+  return plan_impl(n, k, dtype, aligned, sm_count, forced, out);
+}
+
+extern "C" int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cudaStream_t stream) {
+  if (dtype < 0 || dtype > 3) return GEMV_ERR_DTYPE;
+  if (n < 0 || k < 0 || k > INT32_MAX) return GEMV_ERR_ARG;
+  if (n == 0 || k == 0) return GEMV_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  const bool aligned = b_aligned16 != 0 && k % 8 == 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const DeviceInfo &di = device_info_locked(dev);
+  if (!di.ok) return GEMV_ERR_DEVICE;
+  Key key{dev, dtype, aligned ? 1 : 0, n, k};
+  gemv_config cfg{};
+  auto it = g_cache.find(key);
+  if (it != g_cache.end()) {
+    cfg = it->second;
+  } else {
+    int st = plan_impl(n, k, dtype, aligned, di.sm_count, nullptr, &cfg);
+    if (st != GEMV_OK) return st;
+    g_cache.emplace(key, cfg);
+  }
+  MainKernel mk = lookup_main(dtype, cfg);
+  if (mk == nullptr) return GEMV_ERR_CONFIG;
+  cudaError_t e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cfg.grid_split > 1) {
+    float *ws = nullptr;
+    return workspace_locked(dev, stream, (size_t)cfg.grid_split * (size_t)n * sizeof(float), &ws);
+  }
+  return GEMV_OK;
+}
+
+extern "C" int gemv_last_config(gemv_config *out) {
+  if (out == nullptr) return GEMV_ERR_ARG;
+  if (!t_has_last) return GEMV_ERR_ARG;
+  *out = t_last;
+  return GEMV_OK;
+}
+
+extern "C" const char *gemv_status_string(int status) {
+  switch (status) {
+    case GEMV_OK: return "ok";
+    case GEMV_ERR_ARG: return "invalid argument (null pointer, negative or oversized n/k)";
+    case GEMV_ERR_DTYPE: return "unknown dtype code";
+    case GEMV_ERR_ALIAS: return "output c overlaps input B or a";
+    case GEMV_ERR_DEVICE: return "no usable device (current device must be sm_103)";
+    case GEMV_ERR_CUDA: return "a CUDA call or kernel launch failed (see gemv_last_cuda_error)";
+    case GEMV_ERR_CONFIG: return "configuration invalid for this shape";
+    case GEMV_ERR_ALIGN: return "pointer not aligned to its element type";
+    case GEMV_ERR_NOMEM: return "split-K workspace allocation failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int gemv_last_cuda_error(void) { return t_cuda_err; }
+
+extern "C" int gemv_debug_inject(int status) {
+  g_inject.store(status);
+  return GEMV_OK;
+}
+
+extern "C" int gemv_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (auto &kv : g_ws) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  if (cur >= 0) cudaSetDevice(cur);
+  cudaGetLastError();
+  g_ws.clear();
+  g_cache.clear();
+  return GEMV_OK;
+}
+
+extern "C" int gemv_host(const void *B_host, const void *a_host, void *c_host, void *B_dev, void *a_dev,
+                         void *c_dev, int64_t n, int64_t k, int dtype, cudaStream_t stream) {
+  int inj = g_inject.exchange(0);
+  if (inj != 0) return inj;
+  int st = validate(B_dev, a_dev, c_dev, n, k, dtype);
+  if (st != GEMV_OK) return st;
+  if (n == 0) return GEMV_OK;
+  if (c_host == nullptr || (k > 0 && (B_host == nullptr || a_host == nullptr))) return GEMV_ERR_ARG;
+  cudaError_t e;
+  if (k > 0) {
+    e = cudaMemcpyAsync(B_dev, B_host, (size_t)n * (size_t)k * 2, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemcpyAsync(a_dev, a_host, (size_t)k * 2, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  st = run(B_dev, a_dev, c_dev, n, k, dtype, nullptr, stream);
+  if (st != GEMV_OK) return st;
+  e = cudaMemcpyAsync(c_host, c_dev, (size_t)n * out_elem_bytes(dtype), cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GEMV_OK;
+}
+
+extern "C" int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t stream) {
+  if (buf == nullptr || sink == nullptr || bytes <= 0) return GEMV_ERR_ARG;
+  if (((uintptr_t)buf & 15u) || (bytes & 15) || ((uintptr_t)sink & 3u)) return GEMV_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  int sms;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const DeviceInfo &di = device_info_locked(dev);
+    if (!di.ok) return GEMV_ERR_DEVICE;
+    sms = di.sm_count;
+  }
+  ProbeKernel pk = probe_kernel();
+  int per_sm = 0;
+  cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)pk, 512, 0);
+  if (oe != cudaSuccess) return cuda_fail(oe);
+  int grid = sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > kProbeSinkWords) grid = kProbeSinkWords;
+  pk<<<grid, 512, 0, stream>>>(static_cast<const uint4 *>(buf), bytes / 16, static_cast<uint32_t *>(sink));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GEMV_OK;
+}

@@ -1,0 +1,43 @@
+// Internal declarations shared by the host API and the kernel translation
+// units of the GEMV library.  Not installed; the public surface is gemv.h.
+#pragma once
+
+#include <stdint.h>
+
+namespace gemvk {
+
+// Launch parameters of the main streaming kernel (passed by value).
+struct Params {
+  const uint16_t *B;  // n x k row-major, element (2-byte) aligned
+  const uint16_t *a;  // k elements
+  void *c;            // output, when grid_split == 1
+  float *ws;          // fp32 partials ws[s * n + row], when grid_split > 1
+  int64_t n;
+  int64_t k;
+  int64_t kseg;       // columns per k-segment
+  int32_t base_off;   // (address of B / 2) mod 8: B's element offset within a 16-byte block
+  int32_t sg;         // grid split (CTAs per row block)
+  int32_t sw;         // warp split (warps per row inside a CTA)
+  int32_t nrb;        // row blocks = gridDim.x / sg
+  int32_t as_elems;   // staged a elements per CTA (multiple of 8, >= kseg + 24)
+};
+
+typedef void (*MainKernel)(Params);
+typedef void (*ReduceKernel)(const float *, void *, int64_t, int32_t);
+typedef void (*ProbeKernel)(const uint4 *, int64_t, uint32_t *);
+
+// Kernel lookup.  in16: 0 fp16, 1 bf16.  out_f32: 0 same as input, 1 fp32.
+// variant: 1 aligned rows, 2 general rows.  R: rows per warp.
+// Returns nullptr for a combination that is not instantiated.
+MainKernel main_kernel_f16(int out_f32, int variant, int R);
+MainKernel main_kernel_bf16(int out_f32, int variant, int R);
+ReduceKernel reduce_kernel_f16(int out_f32);
+ReduceKernel reduce_kernel_bf16(int out_f32);
+ProbeKernel probe_kernel();
+
+// Loads per lane issued back to back (per row) for R rows per warp.
+inline int unroll_for_rows(int R) { return R == 1 ? 8 : (R == 2 ? 4 : 2); }
+
+constexpr int kMaxThreads = 512;  // launch bound of the main kernel
+
+}  // namespace gemvk

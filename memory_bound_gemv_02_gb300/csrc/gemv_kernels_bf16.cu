@@ -1,0 +1,4 @@
+// bf16 instantiations of the streaming GEMV kernels.
+#include "gemv_kernels.cuh"
+
+GEMV_DEFINE_KERNEL_TABLE(BF16, bf16)

@@ -1,0 +1,104 @@
+"""A host-side model of the streaming kernel's index arithmetic.
+
+It replays, for a configuration from the planner, exactly the row, segment
+and 16-byte-block ranges each CTA and warp of ``gemv_rows_kernel`` touches,
+and the shared-memory, partial-sum and workspace indices it uses, so that the
+following can be checked on the CPU before any launch:
+
+* every element B[i, j] contributes exactly once (masked elements excluded);
+* every global 16-byte block read lies inside the blocks that hold B;
+* every shared-memory vector read lies inside the staged a segment, and the
+  staged element read for (i, j) is a[j];
+* cross-warp partial and split-K workspace indices stay in their buffers.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _row_range(rbk, n, nrb):
+    q, rem = divmod(n, nrb)
+    r0 = rbk * q + min(rbk, rem)
+    return r0, r0 + q + (1 if rbk < rem else 0)
+
+
+def replay(n, k, cfg, base_off=0):
+    """Return a dict of findings; raises AssertionError on any violation."""
+    W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
+    nrb, kseg, variant, ctas = cfg["row_blocks"], cfg["k_segment"], cfg["variant"], cfg["ctas"]
+    assert ctas == nrb * Sg and W % Sw == 0
+    as_elems = -(-(kseg + 24) // 8) * 8
+    assert cfg["smem_bytes"] == as_elems * 2 + W * R * 4
+    cover = np.zeros((n, k), dtype=np.int32)
+    total_elems = base_off + n * k  # elements from the aligned base
+    nblocks = -(-total_elems // 8)  # 16-byte blocks that hold any byte of B
+    ws_rows = set()
+    slots = W // Sw
+    for cta in range(ctas):
+        gs, rbk = cta % Sg, cta // Sg
+        r0, r1 = _row_range(rbk, n, nrb)
+        j0 = gs * kseg
+        seglen = min(k - j0, kseg)
+        assert seglen >= 1, "empty k-segment"
+        if Sg > 1:
+            assert j0 % 8 == 0
+        for base in range(r0, r1, slots * R):
+            for warp in range(W):
+                slot, s = divmod(warp, Sw)
+                i0 = base + slot * R
+                if Sw > 1:
+                    for r in range(R):
+                        assert 0 <= (slot * R + r) * Sw + s < W * R
+                if variant == 1:
+                    assert base_off == 0 and k % 8 == 0 and seglen % 8 == 0
+                    nt = seglen // 8
+                    t0, t1 = nt * s // Sw, nt * (s + 1) // Sw
+                    if t1 <= t0:
+                        continue
+                    t = np.arange(t0, t1)
+                    assert ((t + 1) * 8 + 7 < as_elems).all()
+                    for r in range(R):
+                        row = i0 + r if i0 + r < r1 else i0  # rows past r1 re-read row i0
+                        if i0 >= r1:
+                            break
+                        blk = (row * k + j0) // 8 + t
+                        assert blk.min() >= 0 and blk.max() < nblocks
+                        if i0 + r < r1:
+                            cols = (j0 + 8 * t[:, None] + np.arange(8)[None, :]).ravel()
+                            np.add.at(cover[row], cols, 1)
+                else:
+                    assert R == 1
+                    if i0 >= r1:
+                        continue
+                    e0 = base_off + i0 * k + j0
+                    g0, off = e0 >> 3, e0 & 7
+                    nt = (off + seglen + 7) >> 3
+                    t0, t1 = nt * s // Sw, nt * (s + 1) // Sw
+                    if t1 <= t0:
+                        continue
+                    last_hi = seglen + off - 8 * (nt - 1)
+                    assert 1 <= last_hi <= 8
+                    t = np.arange(t0, t1)
+                    blk = g0 + t
+                    assert blk.min() >= 0 and blk.max() < nblocks
+                    assert ((t + 1) * 8 + 7 < as_elems).all()  # as4[t + 1] (and as4[t]) in range
+                    p = np.arange(8)[None, :]
+                    tt = t[:, None]
+                    valid = ((tt > 0) | (p >= off)) & ((tt < nt - 1) | (p < last_hi))
+                    # staged index of element p of block t, and the column it holds
+                    x = 8 * tt + (8 - off) + p
+                    col_from_stage = j0 + x - 8
+                    elem = 8 * blk[:, None] + p - base_off  # flat element index in B
+                    col_from_B = elem - i0 * k
+                    assert (col_from_stage[valid] == col_from_B[valid]).all()
+                    assert (x[valid] >= 8).all() and (x[valid] < 8 + seglen).all()
+                    np.add.at(cover[i0], col_from_B[valid], 1)
+        if Sg > 1:
+            for row in range(r0, r1):
+                idx = gs * n + row
+                assert 0 <= idx < Sg * n
+                ws_rows.add(idx)
+    assert (cover == 1).all(), f"coverage wrong: min {cover.min()} max {cover.max()}"
+    if Sg > 1:
+        assert len(ws_rows) == Sg * n
+    return {"ctas": ctas}

@@ -1,0 +1,241 @@
+"""Bitwise checks of the CUDA path (closed forms and integer-valued inputs),
+ragged tails, offset pointers, edge cases, error paths and determinism.
+
+With B and a integer-valued in {-3..3} every fp32 partial sum is an integer
+below 2^24, hence exact in any order: the output must then equal the
+oracle's value rounded once to the output format, bit for bit, whatever the
+variant, split or alignment.  That pins tails, split-K and the general
+(realigning) variant exactly.
+"""
+from __future__ import annotations
+
+import itertools
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_gemv_02_gb300 as g
+import oracle
+from gpu_helpers import check_against_oracle, exact_bits_match, oracle_for
+from memory_bound_gemv_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [None, {"variant": 2}, {"rows_per_warp": 4}, {"warps_per_cta": 4, "warp_split": 4},
+           {"grid_split": 3}, {"grid_split": 2, "warp_split": 8}, {"ctas": 3}]
+
+
+def _run(B, a, out_fp32=False, config=None, c=None):
+    if config:
+        return g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=config)
+    return g.gemv(B, a, c=c, out_fp32=out_fp32)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("k", [1, 7, 8, 4096, 7169, 16384])
+def test_ones_give_k(cuda_dev, dtype, k):
+    B = torch.ones((37, k), dtype=inputs.TORCH_DTYPE[dtype], device=cuda_dev)
+    a = torch.ones(k, dtype=B.dtype, device=cuda_dev)
+    c32 = _run(B, a, True)
+    assert (c32.cpu() == float(k)).all()  # exact in fp32
+    c = _run(B, a, False)
+    want = oracle.round_out(np.full(37, float(k)), dtype)
+    assert (inputs.out_bits(c) == want).all()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("n,k", [(64, 100), (100, 64), (33, 33), (5, 4099)])
+def test_identity_padded_gives_a(cuda_dev, dtype, n, k):
+    B = torch.zeros((n, k), dtype=inputs.TORCH_DTYPE[dtype], device=cuda_dev)
+    m = min(n, k)
+    B[torch.arange(m), torch.arange(m)] = 1
+    _, a = inputs.make_inputs(1, k, dtype, "uniform", 2, cuda_dev)
+    for cfg in CONFIGS:
+        c = _run(B, a, False, cfg)
+        want = torch.zeros(n, dtype=B.dtype, device=cuda_dev)
+        want[:m] = a[:m]
+        assert (inputs.out_bits(c) == inputs.out_bits(want)).all(), cfg
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("out_fp32", [False, True])
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_integer_inputs_bit_exact(cuda_dev, dtype, out_fp32, cfg):
+    for n, k in [(1, 1), (3, 9), (17, 31), (129, 257), (1000, 7169), (513, 4096), (64, 16384)]:
+        B, a = inputs.make_int_inputs(n, k, dtype, seed=n + k, device=cuda_dev)
+        try:
+            c = _run(B, a, out_fp32, cfg)
+        except g.GemvError as e:
+            assert e.status == g.GEMV_ERR_CONFIG
+            continue
+        assert exact_bits_match(c, B, a, out_fp32), (n, k, cfg)
+
+
+TAIL_N = [1, 2, 3, 7, 8, 9, 16, 17, 31, 32, 33, 255, 256, 257]
+TAIL_K = [1, 2, 5, 8, 9, 15, 16, 17, 31, 33, 255, 256, 257, 4099]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_ragged_tails_bit_exact(cuda_dev, dtype):
+    for n, k in itertools.product(TAIL_N, TAIL_K):
+        B, a = inputs.make_int_inputs(n, k, dtype, seed=7 * n + k, device=cuda_dev)
+        c = _run(B, a, False)
+        assert exact_bits_match(c, B, a, False), (n, k)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("b_off,a_off", [(1, 0), (0, 1), (3, 5), (7, 7)])
+def test_offset_views_take_the_general_path(cuda_dev, dtype, b_off, a_off):
+    """B and a starting at element offsets (not 16-byte aligned)."""
+    td = inputs.TORCH_DTYPE[dtype]
+    for n, k in [(50, 64), (33, 4096), (9, 7169)]:
+        Bi, ai = inputs.make_int_inputs(n, k, dtype, seed=n, device=cuda_dev)
+        Bbuf = torch.zeros(n * k + 16, dtype=td, device=cuda_dev)
+        abuf = torch.zeros(k + 16, dtype=td, device=cuda_dev)
+        Bv = Bbuf[b_off:b_off + n * k].view(n, k)
+        av = abuf[a_off:a_off + k]
+        Bv.copy_(Bi)
+        av.copy_(ai)
+        c = _run(Bv, av, False)
+        if b_off % 8 or k % 8:
+            assert g.gemv_last_config()["variant"] == g.GEMV_VARIANT_ROWS_GENERAL
+        assert exact_bits_match(c, Bi, ai, False), (n, k, b_off, a_off)
+        Bu, au = inputs.make_inputs(n, k, dtype, "uniform", 9, cuda_dev)
+        Bv.copy_(Bu)
+        av.copy_(au)
+        c = _run(Bv, av, True)
+        check_against_oracle(c, Bu, au, True, label=f"offset {b_off},{a_off} {n}x{k}")
+
+
+def test_output_guard_bands_untouched(cuda_dev):
+    for out_fp32 in (False, True):
+        for cfg in CONFIGS:
+            B, a = inputs.make_inputs(1001, 3001, "bf16", "uniform", 4, cuda_dev)
+            dt = torch.float32 if out_fp32 else torch.bfloat16
+            buf = torch.full((1001 + 256,), 1234.5, dtype=dt, device=cuda_dev)
+            c = buf[128:128 + 1001]
+            _run(B, a, out_fp32, cfg, c=c)
+            torch.cuda.synchronize()
+            assert (buf[:128] == 1234.5).all() and (buf[128 + 1001:] == 1234.5).all(), cfg
+            check_against_oracle(c, B, a, out_fp32, label=f"guard {cfg}")
+
+
+def test_empty_and_degenerate_sizes(cuda_dev):
+    B = torch.empty((0, 64), dtype=torch.float16, device=cuda_dev)
+    a = torch.ones(64, dtype=torch.float16, device=cuda_dev)
+    assert g.gemv(B, a).numel() == 0
+    B = torch.empty((5, 0), dtype=torch.bfloat16, device=cuda_dev)
+    a = torch.empty(0, dtype=torch.bfloat16, device=cuda_dev)
+    c = torch.full((5,), 7.0, dtype=torch.bfloat16, device=cuda_dev)
+    g.gemv(B, a, c=c)
+    torch.cuda.synchronize()
+    assert (inputs.out_bits(c) == 0).all()  # +0: the empty sum
+
+
+def test_nonfinite_inputs_stay_in_their_rows(cuda_dev):
+    for dtype in ("f16", "bf16"):
+        for k in (64, 67):
+            B, a = inputs.make_int_inputs(8, k, dtype, seed=1, device=cuda_dev)
+            B[2, 5] = float("inf")
+            B[5, k - 1] = float("nan")
+            B[6, 0] = float("-inf")
+            for cfg in CONFIGS:
+                c = _run(B, a, True, cfg).cpu()
+                want, _ = oracle_for(B, a)
+                for i in range(8):
+                    if np.isnan(want[i]):
+                        assert torch.isnan(c[i]), (i, cfg)
+                    else:
+                        assert c[i].item() == want[i], (i, cfg, c[i].item(), want[i])
+
+
+def test_error_paths_launch_nothing(cuda_dev):
+    B, a = inputs.make_inputs(64, 128, "f16", "uniform", 0, cuda_dev)
+    with pytest.raises(g.GemvError) as ei:
+        g.gemv(B, a, c=B.view(-1)[:64])  # c inside B
+    assert ei.value.status == g.GEMV_ERR_ALIAS
+    with pytest.raises(g.GemvError) as ei:
+        g.gemv_ex(B, a, config={"grid_split": 100})
+    assert ei.value.status == g.GEMV_ERR_CONFIG
+    g.gemv_debug_inject(g.GEMV_ERR_CUDA)
+    c = torch.full((64,), 3.0, dtype=torch.float16, device=cuda_dev)
+    with pytest.raises(g.GemvError) as ei:
+        g.gemv(B, a, c=c)
+    assert ei.value.status == g.GEMV_ERR_CUDA
+    torch.cuda.synchronize()
+    assert (c == 3.0).all()  # nothing ran
+    g.gemv(B, a, c=c)  # the injected status was one-shot; the context is healthy
+    check_against_oracle(c, B, a, False)
+
+
+def test_determinism_repeated_calls(cuda_dev):
+    """Fixed-order reductions: 200 calls give bitwise-identical results (a
+    race in the cross-warp or split-K combination would show up here)."""
+    for cfg in (None, {"warp_split": 8, "warps_per_cta": 16}, {"grid_split": 4}):
+        B, a = inputs.make_inputs(3001, 5000, "f16", "normal", 2, cuda_dev, b_sigma=0.5)
+        first = _run(B, a, True, cfg).clone()
+        c = torch.empty_like(first)
+        for _ in range(200):
+            _run(B, a, True, cfg, c=c)
+            assert torch.equal(c, first), cfg
+
+
+def test_concurrent_streams_split_k(cuda_dev):
+    """Split-K workspaces are per stream: concurrent calls do not interfere."""
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    data = [inputs.make_inputs(333, 20000, "bf16", "uniform", s, cuda_dev) for s in range(3)]
+    outs = []
+    for s, (B, a) in zip(streams, data):
+        with torch.cuda.stream(s):
+            outs.append(g.gemv_ex(B, a, out_fp32=True, config={"grid_split": 4}, stream=s))
+    torch.cuda.synchronize()
+    for (B, a), c in zip(data, outs):
+        check_against_oracle(c, B, a, True)
+
+
+def test_gemv_host_end_to_end(cuda_dev):
+    n, k = 1000, 3000
+    Bd, ad = inputs.make_inputs(n, k, "f16", "uniform", 3, cuda_dev)
+    Bh = Bd.cpu().pin_memory()
+    ah = ad.cpu().pin_memory()
+    ch = torch.empty(n, dtype=torch.float16).pin_memory()
+    B_dev = torch.empty_like(Bd)
+    a_dev = torch.empty_like(ad)
+    c_dev = torch.empty(n, dtype=torch.float16, device=cuda_dev)
+    g.gemv_host(Bh, ah, ch, B_dev, a_dev, c_dev)
+    torch.cuda.synchronize()
+    check_against_oracle(ch.to(cuda_dev), Bd, ad, False, label="gemv_host")
+
+
+def test_probe_checksum(cuda_dev):
+    buf = torch.randint(-2 ** 31, 2 ** 31 - 1, (1 << 22,), dtype=torch.int32, device=cuda_dev)
+    sink = torch.zeros(16384, dtype=torch.int32, device=cuda_dev)
+    g.gemv_probe_read(buf, sink)
+    torch.cuda.synchronize()
+    x = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))
+    y = np.bitwise_xor.reduce(buf.cpu().numpy().view(np.uint32))
+    assert x == y
+
+
+def test_host_overhead_per_call(cuda_dev):
+    """A cached-key call costs microseconds of host time (the pages' Case B.4
+    saw 11 ms per call from rebuilding a closure).  Measured on the raw
+    C entry point with enqueue-only timing."""
+    B, a = inputs.make_inputs(256, 512, "f16", "uniform", 0, cuda_dev)
+    c = torch.empty(256, dtype=torch.float16, device=cuda_dev)
+    L = g.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    args = (B.data_ptr(), a.data_ptr(), c.data_ptr(), 256, 512, 0, s)
+    assert L.gemv(*args) == 0
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(20):
+        t0 = time.perf_counter()
+        for _ in range(200):  # bursts short enough never to fill the launch queue
+            L.gemv(*args)
+        per.append((time.perf_counter() - t0) / 200)
+        torch.cuda.synchronize()
+    med = float(np.median(per))
+    assert med < 10e-6, f"host time per call {med * 1e6:.2f} us"

@@ -1,0 +1,123 @@
+"""The planner (a pure host function of the C library) and the kernel's index
+arithmetic, checked on the CPU for every workload shape and for forced
+configurations, before anything runs on a GPU."""
+from __future__ import annotations
+
+import itertools
+
+import pytest
+
+import kernel_model
+
+SM = 152  # GB300; the planner takes the SM count as an argument
+WORKLOADS = [
+    (256, 512), (7168, 16384), (18432, 7168), (4096, 4096), (14336, 4096), (4096, 14336),
+    (28672, 8192), *itertools.product([1024, 4099, 18433, 65536], [1000, 4096, 7169, 16384]),
+    (57344, 7168), (1, 1), (1, 7), (3, 9), (1, 100000), (2, 2 ** 20), (100000, 8),
+]
+MAX_SMEM = 232448
+
+
+@pytest.mark.parametrize("n,k", WORKLOADS)
+@pytest.mark.parametrize("dtype", [0, 1, 2, 3])
+@pytest.mark.parametrize("aligned", [True, False])
+@pytest.mark.parametrize("sm", [SM, 148])
+def test_plan_invariants(gemv_lib, n, k, dtype, aligned, sm):
+    cfg = gemv_lib.gemv_plan(n, k, dtype, aligned, sm)
+    W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
+    assert W in (4, 8, 16) and R in (1, 2, 4) and W % Sw == 0
+    assert cfg["variant"] == (1 if aligned and k % 8 == 0 else 2)
+    if cfg["variant"] == 2:
+        assert R == 1
+    kseg = cfg["k_segment"]
+    assert Sg * kseg >= k and (Sg - 1) * kseg < k
+    if Sg > 1:
+        assert kseg % 8 == 0
+    assert cfg["ctas"] == cfg["row_blocks"] * Sg >= 1
+    assert cfg["smem_bytes"] <= MAX_SMEM
+    assert cfg["launches"] == (2 if Sg > 1 else 1)
+    # persistent grid: never more CTAs than can be resident at once
+    cps = min(32 // W, 233472 // (cfg["smem_bytes"] + 1024))
+    assert cfg["ctas"] <= max(sm * cps, Sg)
+
+
+def test_plan_shapes_of_interest(gemv_lib):
+    big = gemv_lib.gemv_plan(7168, 16384, 0, True, SM)
+    assert big["grid_split"] == 1 and big["warp_split"] == 1 and big["variant"] == 1
+    tiny_n = gemv_lib.gemv_plan(16, 16384, 0, True, SM)
+    assert tiny_n["warp_split"] * tiny_n["grid_split"] > 1  # rows are split to fill the GPU
+    huge_k = gemv_lib.gemv_plan(2, 2 ** 20, 1, True, SM)
+    assert huge_k["grid_split"] >= 32 and huge_k["k_segment"] <= 32768
+
+
+@pytest.mark.parametrize("cfg", [
+    {"variant": 1, "rows_per_warp": 4}, {"warps_per_cta": 4, "warp_split": 4},
+    {"grid_split": 3}, {"warps_per_cta": 8, "warp_split": 2, "grid_split": 2},
+    {"ctas": 7}, {"ctas": 1}, {"warps_per_cta": 16, "warp_split": 16},
+])
+def test_forced_configs_are_honoured(gemv_lib, cfg):
+    out = gemv_lib.gemv_plan(1000, 4096, 0, True, SM, config=cfg)
+    for key, v in cfg.items():
+        if key == "ctas":
+            assert out["ctas"] == (v // out["grid_split"]) * out["grid_split"]
+        else:
+            assert out[key] == v
+
+
+@pytest.mark.parametrize("cfg", [
+    {"variant": 3}, {"rows_per_warp": 3}, {"warps_per_cta": 12}, {"warps_per_cta": 8, "warp_split": 3},
+    {"grid_split": 65}, {"variant": 2, "rows_per_warp": 2},
+])
+def test_invalid_forced_configs_rejected(gemv_lib, cfg):
+    with pytest.raises(gemv_lib.GemvError) as ei:
+        gemv_lib.gemv_plan(1000, 4096, 0, True, SM, config=cfg)
+    assert ei.value.status == gemv_lib.GEMV_ERR_CONFIG
+
+
+def test_aligned_variant_refused_for_ragged_k(gemv_lib):
+    with pytest.raises(gemv_lib.GemvError):
+        gemv_lib.gemv_plan(100, 4097, 0, True, SM, config={"variant": 1})
+    with pytest.raises(gemv_lib.GemvError):
+        gemv_lib.gemv_plan(100, 4096, 0, False, SM, config={"variant": 1})
+
+
+# ------------------------------------------------ index-arithmetic replay --
+
+SMALL = [(1, 1), (1, 8), (2, 7), (3, 9), (5, 17), (13, 31), (17, 64), (33, 100), (64, 512), (7, 1000),
+         (40, 257), (129, 33), (3, 4099)]
+
+
+@pytest.mark.parametrize("n,k", SMALL)
+@pytest.mark.parametrize("base_off", [0, 1, 3, 7])
+@pytest.mark.parametrize("forced", [None, {"warps_per_cta": 4, "warp_split": 2},
+                                    {"grid_split": 3}, {"warps_per_cta": 8, "warp_split": 4, "grid_split": 2},
+                                    {"ctas": 3}, {"warps_per_cta": 16, "warp_split": 16}])
+def test_general_variant_index_replay(gemv_lib, n, k, base_off, forced):
+    try:
+        cfg = gemv_lib.gemv_plan(n, k, 0, False, SM, config=forced)
+    except gemv_lib.GemvError:
+        pytest.skip("configuration not valid for this shape")
+    assert cfg["variant"] == 2
+    kernel_model.replay(n, k, cfg, base_off=base_off)
+
+
+@pytest.mark.parametrize("n,k", [(1, 8), (3, 16), (5, 64), (17, 256), (64, 512), (33, 1000), (7, 4096),
+                                 (129, 40), (300, 24)])
+@pytest.mark.parametrize("forced", [None, {"rows_per_warp": 2}, {"rows_per_warp": 4},
+                                    {"rows_per_warp": 4, "warps_per_cta": 4, "warp_split": 2},
+                                    {"grid_split": 3}, {"ctas": 2, "rows_per_warp": 2},
+                                    {"warps_per_cta": 16, "warp_split": 8, "grid_split": 2}])
+def test_aligned_variant_index_replay(gemv_lib, n, k, forced):
+    try:
+        cfg = gemv_lib.gemv_plan(n, k, 1, True, SM, config=forced)
+    except gemv_lib.GemvError:
+        pytest.skip("configuration not valid for this shape")
+    assert cfg["variant"] == 1
+    kernel_model.replay(n, k, cfg, base_off=0)
+
+
+@pytest.mark.parametrize("n,k,aligned", [(256, 512, True), (1024, 1000, True), (4099, 1000, True),
+                                         (1024, 7169, False), (300, 7169, False)])
+def test_planner_choice_replay_medium(gemv_lib, n, k, aligned):
+    cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM)
+    kernel_model.replay(n, k, cfg, base_off=0 if aligned else 3)
