@@ -177,7 +177,8 @@ __device__ __forceinline__ void store_out(const Params &p, int gs, int64_t row, 
 template <class T, int R, int U>
 __device__ __forceinline__ void rows_aligned(const Params &p, const uint4 *as4, int64_t i0, int64_t r1,
                                              int64_t j0, int t0, int t1, int lane, float (&out)[R]) {
-  // Rows past r1 (only in the CTA's last group) re-read row i0 and are discarded.
+  // Called with i0 < r1.  Rows past r1 (only in the CTA's last group)
+  // re-read row i0 and their sums are discarded.
   const uint4 *b0 = reinterpret_cast<const uint4 *>(p.B + i0 * p.k + j0);
   const int kv = (int)(p.k >> 3);  // row stride in 16-byte vectors
   int roff[R];
@@ -311,7 +312,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_rows_kernel(Params p) {
     if constexpr (ALIGNED) {
       const int nt = (int)(len >> 3);
       const int t0 = (int)((int64_t)nt * s / sw), t1 = (int)((int64_t)nt * (s + 1) / sw);
-      rows_aligned<T, R, U>(p, as4, i0, r1, j0, t0, t1, lane, v);
+      if (i0 < r1) {  // warp-uniform; a slot past the CTA's rows reads nothing
+        rows_aligned<T, R, U>(p, as4, i0, r1, j0, t0, t1, lane, v);
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] = 0.f;
+      }
     } else {
       v[0] = (i0 < r1) ? row_general_dispatch<T, U>(p, as4, i0, j0, len, s, sw, lane) : 0.f;
     }

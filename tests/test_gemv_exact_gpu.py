@@ -33,6 +33,16 @@ def _run(B, a, out_fp32=False, config=None, c=None):
     return g.gemv(B, a, c=c, out_fp32=out_fp32)
 
 
+def _run_valid(B, a, out_fp32=False, config=None, c=None):
+    """As _run, but None when the forced configuration does not apply to
+    this shape (e.g. several rows per warp with k % 8 != 0)."""
+    try:
+        return _run(B, a, out_fp32, config, c)
+    except g.GemvError as e:
+        assert e.status == g.GEMV_ERR_CONFIG
+        return None
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("k", [1, 7, 8, 4096, 7169, 16384])
 def test_ones_give_k(cuda_dev, dtype, k):
@@ -53,7 +63,9 @@ def test_identity_padded_gives_a(cuda_dev, dtype, n, k):
     B[torch.arange(m), torch.arange(m)] = 1
     _, a = inputs.make_inputs(1, k, dtype, "uniform", 2, cuda_dev)
     for cfg in CONFIGS:
-        c = _run(B, a, False, cfg)
+        c = _run_valid(B, a, False, cfg)
+        if c is None:
+            continue
         want = torch.zeros(n, dtype=B.dtype, device=cuda_dev)
         want[:m] = a[:m]
         assert (inputs.out_bits(c) == inputs.out_bits(want)).all(), cfg
@@ -65,10 +77,8 @@ def test_identity_padded_gives_a(cuda_dev, dtype, n, k):
 def test_integer_inputs_bit_exact(cuda_dev, dtype, out_fp32, cfg):
     for n, k in [(1, 1), (3, 9), (17, 31), (129, 257), (1000, 7169), (513, 4096), (64, 16384)]:
         B, a = inputs.make_int_inputs(n, k, dtype, seed=n + k, device=cuda_dev)
-        try:
-            c = _run(B, a, out_fp32, cfg)
-        except g.GemvError as e:
-            assert e.status == g.GEMV_ERR_CONFIG
+        c = _run_valid(B, a, out_fp32, cfg)
+        if c is None:
             continue
         assert exact_bits_match(c, B, a, out_fp32), (n, k, cfg)
 
@@ -116,7 +126,8 @@ def test_output_guard_bands_untouched(cuda_dev):
             dt = torch.float32 if out_fp32 else torch.bfloat16
             buf = torch.full((1001 + 256,), 1234.5, dtype=dt, device=cuda_dev)
             c = buf[128:128 + 1001]
-            _run(B, a, out_fp32, cfg, c=c)
+            if _run_valid(B, a, out_fp32, cfg, c=c) is None:
+                continue
             torch.cuda.synchronize()
             assert (buf[:128] == 1234.5).all() and (buf[128 + 1001:] == 1234.5).all(), cfg
             check_against_oracle(c, B, a, out_fp32, label=f"guard {cfg}")
@@ -142,7 +153,10 @@ def test_nonfinite_inputs_stay_in_their_rows(cuda_dev):
             B[5, k - 1] = float("nan")
             B[6, 0] = float("-inf")
             for cfg in CONFIGS:
-                c = _run(B, a, True, cfg).cpu()
+                c = _run_valid(B, a, True, cfg)
+                if c is None:
+                    continue
+                c = c.cpu()
                 want, _ = oracle_for(B, a)
                 for i in range(8):
                     if np.isnan(want[i]):
