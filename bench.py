@@ -24,6 +24,7 @@ cores on a bounded sample of rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import csv
 import hashlib
 import io
@@ -323,6 +324,7 @@ def time_calls(L, calls, stream, steps, warmup):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s = torch.cuda.current_stream()
+    torch.cuda._sleep(3_000_000)  # keep the GPU busy while the launches queue up
     e0.record(s)
     for i in range(steps):
         fn, args = calls[i % len(calls)]
@@ -400,6 +402,26 @@ def run_sweep(args, dev):
     return 0
 
 
+def run_case(args, dev):
+    """Run one shape a few times and exit (for profiler captures):
+    --case N,K,DTYPE[,f32] [--calls C] [--config JSON]."""
+    import torch
+
+    import memory_bound_gemv_02_gb300 as g
+    from memory_bound_gemv_02_gb300 import inputs
+    parts = args.case.split(",")
+    n, k, dtype = int(parts[0]), int(parts[1]), parts[2]
+    out_fp32 = len(parts) > 3 and parts[3] == "f32"
+    B, a = inputs.make_inputs(n, k, dtype, "normal", 0, dev)
+    c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
+    cfg = json.loads(args.config) if args.config else None
+    for _ in range(args.calls):
+        g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=cfg)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": args.case, "calls": args.calls, "config": g.gemv_last_config()}))
+    return 0
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -414,6 +436,8 @@ def run_ours(args, world, rank, local):
     L = g.lib()
     if args.sweep:
         return run_sweep(args, dev)
+    if args.case:
+        return run_case(args, dev)
 
     w = WORKLOAD
     n, k, fmt = w["n"], w["k"], w["dtype"]
@@ -429,7 +453,13 @@ def run_ours(args, world, rank, local):
     g.gemv(B, a, c=c, out_fp32=w["out_fp32"])
     torch.cuda.synchronize()
     cfg = g.gemv_last_config()
-    calls = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in (B, B2)]
+    # The timed calls are launched back to back with programmatic dependent
+    # launch and the first B tile read before the wait (B is the read-only
+    # weight matrix; a and c are ordered after the previous call).
+    overlap_cfg = g.GemvConfig()
+    overlap_cfg.overlap = g.GEMV_OVERLAP_PDL_PREFETCH_B
+    ocfg = ctypes.byref(overlap_cfg)
+    calls = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ocfg, s)) for Bx in (B, B2)]
 
     # timed region
     for i in range(args.warmup):
@@ -437,8 +467,7 @@ def run_ours(args, world, rank, local):
         if fn(*cargs) != 0:
             raise RuntimeError("gemv failed in warm-up")
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(dev)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
     with ClockSampler(gpu_id) as clk:
@@ -446,24 +475,38 @@ def run_ours(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize()
         t_host0 = time.time()
-        t0 = time.perf_counter()
+        ev0.record(stream)
         for i in range(args.steps):
             fn, cargs = calls[i % 2]
-            starts[i].record(stream)
             fn(*cargs)
-            ends[i].record(stream)
+        ev1.record(stream)
         torch.cuda.synchronize()
-        elapsed = time.perf_counter() - t0
         t_host1 = time.time()
         barrier(world)
         time.sleep(0.25)
     clocks = clk.summary(t_host0, t_host1)
-    per = [x.elapsed_time(y) for x, y in zip(starts, ends)]  # ms per launch
+    elapsed = ev0.elapsed_time(ev1) / 1e3
     elapsed_max = max_over_ranks(elapsed, world)
     value = world * nbytes * args.steps / elapsed_max / 1e9
-    mean_launch_ms = sum(per) / len(per)
+    mean_launch_ms = elapsed / args.steps * 1e3  # average launch duration over the timed region
     achieved = nbytes / (mean_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
+
+    # Context (untimed for `value`): the same calls without overlap, back to
+    # back, and one at a time with CUDA events around each launch.
+    plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in (B, B2)]
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(3_000_000)
+    e_a.record(stream)
+    nplain = min(args.steps, 2000)
+    for i in range(nplain):
+        fn, cargs = plain[i % 2]
+        fn(*cargs)
+    e_b.record(stream)
+    torch.cuda.synchronize()
+    us_plain = e_a.elapsed_time(e_b) * 1e3 / nplain
+    _, per_iso = time_calls(L, plain, s, 200, 10)
+    us_iso = statistics.median(per_iso) * 1e3
 
     # e2e through the C-ABI from pinned host buffers (H2D of B and a, D2H of c)
     Bh = B.cpu().pin_memory()
@@ -489,7 +532,7 @@ def run_ours(args, world, rank, local):
     # read-only probe (same load path) for context
     sink = torch.zeros(16384, dtype=torch.int32, device=dev)
     probe_calls = [(L.gemv_probe_read, (Bx.data_ptr(), n * k * 2, sink.data_ptr(), s)) for Bx in (B, B2)]
-    _, pper = time_calls(L, probe_calls, s, 200, 10)
+    _, pper = time_calls(L, probe_calls, s, 100, 10)
     probe_gbs = n * k * 2 / (statistics.median(pper) / 1e3) / 1e9
 
     host_us = host_overhead_us(L, 256, 512, 0, dev, s)
@@ -504,11 +547,13 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD_DESC, "n": n, "k": k, "in_dtype": fmt,
                    "out_dtype": "f32" if w["out_fp32"] else fmt,
                    "l2": "inputs larger than L2: calls alternate two 235 MB copies of B (L2 is 129 MB)",
-                   "launch": {kk: cfg[kk] for kk in ("variant", "rows_per_warp", "warps_per_cta",
-                                                      "warp_split", "grid_split", "ctas", "smem_bytes")},
+                   "launch": {**{kk: cfg[kk] for kk in ("variant", "rows_per_warp", "warps_per_cta", "warp_split",
+                                                         "grid_split", "ctas", "smem_bytes", "unroll")},
+                              "overlap": "programmatic dependent launch, first B tile read before the wait"},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_call": round(mean_launch_ms * 1e3, 3),
-        "us_per_call_median": round(statistics.median(per) * 1e3, 3),
+        "us_per_call_no_overlap": round(us_plain, 3),
+        "us_per_call_isolated_median": round(us_iso, 3),
         "pct_of_nominal_8tbps": round(100 * achieved / NOMINAL_HBM_GBS, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(frac_of_peak(achieved, peak), 4), "peak_kind": f"of {peak_kind}",
@@ -537,6 +582,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None, help="write one JSON line per workload shape here")
     ap.add_argument("--sweep-steps", type=int, default=300)
+    ap.add_argument("--case", default=None, help="N,K,DTYPE[,f32]: run that shape --calls times, no timing")
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--config", default=None, help="JSON launch configuration forced with --case")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -62,9 +62,27 @@ enum {
   GEMV_VARIANT_AUTO = 0,         /* let the planner choose */
   GEMV_VARIANT_ROWS = 1,         /* rows stream as aligned 16-byte vectors; needs k % 8 == 0
                                     and B 16-byte aligned */
-  GEMV_VARIANT_ROWS_GENERAL = 2  /* any k and any 2-byte-aligned B: each row is read as the
+  GEMV_VARIANT_ROWS_GENERAL = 2, /* any k and any 2-byte-aligned B: each row is read as the
                                     aligned 16-byte blocks covering it, edge elements masked,
                                     and a is realigned in registers by the row's offset */
+  GEMV_VARIANT_TILES = 3         /* any alignment: CTAs take interleaved tiles of rows of one
+                                    residue class (row index mod 8, so one block offset per
+                                    CTA), a is staged pre-shifted, rows are split into
+                                    warp_split slices combined in shared memory */
+};
+
+/* Launch overlap with the preceding work on the stream (gemv_config.overlap). */
+enum {
+  GEMV_OVERLAP_NONE = 0,      /* ordinary stream-ordered launch */
+  GEMV_OVERLAP_PDL = 1,       /* programmatic dependent launch: the kernel may be scheduled
+                                 while the preceding kernel drains; it waits for that
+                                 kernel's completion (and its memory) before reading or
+                                 writing any global memory */
+  GEMV_OVERLAP_PDL_PREFETCH_B = 2 /* as GEMV_OVERLAP_PDL, and each CTA streams its first tile
+                                 of B into registers before waiting.  The caller guarantees
+                                 that no work still running on the stream writes B (true
+                                 for weights); a and c are still accessed only after the
+                                 wait */
 };
 
 /*
@@ -74,7 +92,8 @@ enum {
  *  variant        GEMV_VARIANT_*.
  *  rows_per_warp  R: rows one warp streams side by side (1, 2 or 4; 1 for
  *                 the general variant).  The a-vector chunk read from shared
- *                 memory is reused across the R rows.
+ *                 memory is reused across the R rows.  Tiles variant:
+ *                 (R, unroll) is one of (1, 8), (1, 4), (2, 4), (4, 2).
  *  warps_per_cta  W: 4, 8 or 16 warps per CTA.
  *  warp_split     Sw: warps of one CTA that share a row, each streaming a
  *                 contiguous slice of it; their partial sums are combined
@@ -82,13 +101,19 @@ enum {
  *  grid_split     Sg: CTAs that share a block of rows, each over one k-segment.
  *                 Sg > 1 writes fp32 partials to a workspace and launches a
  *                 second kernel that adds them in segment order (split-K).
- *  ctas           total CTAs of the main kernel (row blocks x Sg).
+ *  ctas           total CTAs of the main kernel (row blocks x Sg).  Tiles
+ *                 variant: row_blocks is the CTA count per k-segment, a
+ *                 multiple of 8 unless k % 8 == 0 and B is 16-byte aligned.
  *  smem_bytes     dynamic shared memory per CTA (the staged a segment plus
  *                 the cross-warp partials).
  *  launches       kernels per call: 1, or 2 with split-K.
  *  k_segment      columns per k-segment (a multiple of 8 except when Sg == 1).
  *  row_blocks     number of row blocks (ctas / grid_split).
- *  unroll         U: 16-byte loads per lane issued back to back per row.
+ *  unroll         U: 16-byte loads per lane issued back to back per row
+ *                 (tiles variant: may be forced together with rows_per_warp).
+ *  overlap        GEMV_OVERLAP_*.  Not part of the cached configuration: a
+ *                 gemv_ex() call that sets only this field launches the
+ *                 cached configuration of gemv() with the requested overlap.
  */
 typedef struct gemv_config {
   int32_t variant;
@@ -102,7 +127,8 @@ typedef struct gemv_config {
   int64_t k_segment;
   int32_t row_blocks;
   int32_t unroll;
-  int32_t reserved[4];
+  int32_t overlap;
+  int32_t reserved[3];
 } gemv_config;
 
 /*

@@ -27,7 +27,8 @@ GEMV_F16, GEMV_BF16, GEMV_F16_OUT_F32, GEMV_BF16_OUT_F32 = 0, 1, 2, 3
 GEMV_OK = 0
 GEMV_ERR_ARG, GEMV_ERR_DTYPE, GEMV_ERR_ALIAS, GEMV_ERR_DEVICE = -1, -2, -3, -4
 GEMV_ERR_CUDA, GEMV_ERR_CONFIG, GEMV_ERR_ALIGN, GEMV_ERR_NOMEM = -5, -6, -7, -8
-GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL = 0, 1, 2
+GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TILES = 0, 1, 2, 3
+GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B = 0, 1, 2
 
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
 ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_prepare", "gemv_plan", "gemv_last_config",
@@ -42,7 +43,8 @@ class GemvConfig(ctypes.Structure):
                 ("grid_split", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("k_segment", ctypes.c_int64), ("row_blocks", ctypes.c_int32),
-                ("unroll", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("unroll", ctypes.c_int32), ("overlap", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
 
     def to_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}

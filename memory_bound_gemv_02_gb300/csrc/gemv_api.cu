@@ -27,6 +27,7 @@ namespace {
 
 constexpr int64_t kMaxSegment = 32768;  // columns of a staged per CTA (64 KiB of shared memory)
 constexpr int kMaxGridSplit = 64;
+constexpr int kAutoVariant = GEMV_VARIANT_TILES;  // the planner's default family
 constexpr int kMaxSmemPerCta = 232448;  // 227 KiB, sm_100-family opt-in limit
 constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int64_t kSmemReservedPerCta = 1024;
@@ -118,6 +119,129 @@ const DeviceInfo &device_info_locked(int dev) {
 bool valid_W(int W) { return W == 4 || W == 8 || W == 16; }
 bool valid_R(int R) { return R == 1 || R == 2 || R == 4; }
 
+bool valid_tiles_RU(int R, int U) {
+  return (R == 1 && (U == 8 || U == 4)) || (R == 2 && U == 4) || (R == 4 && U == 2);
+}
+
+// Planner of the tiles variant (pure host arithmetic).
+//  * k-segments: as few as the shared-memory budget allows, more when the
+//    rows alone cannot give every SM work (split-K).
+//  * S (warps per row) so that a slice is at most 32*8 16-byte blocks, i.e.
+//    at most 8 loads per lane; short rows are instead streamed R at a time.
+//  * C (CTAs per segment): every SM busy at 32 resident warps, a multiple
+//    of 8 (one row class per CTA) unless the rows are 16-byte aligned.
+int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f, gemv_config *out) {
+  const int NCLS = aligned ? 1 : 8;
+  const int W_list[3] = {16, 8, 4};
+  gemv_config best{};
+  bool have = false;
+  for (int wi = 0; wi < 3; ++wi) {
+    const int W = f->warps_per_cta ? f->warps_per_cta : W_list[wi];
+    if (!valid_W(W)) return GEMV_ERR_CONFIG;
+    const int cps_warps = 32 / W;
+    // k-segments
+    int64_t Sg = f->grid_split ? f->grid_split : cdiv(k, kMaxSegment);
+    if (Sg < 1 || Sg > kMaxGridSplit) return GEMV_ERR_CONFIG;
+    int64_t kseg = (Sg == 1) ? k : round_up(cdiv(k, Sg), 8);
+    Sg = cdiv(k, kseg);
+    if (kseg > kMaxSegment) return GEMV_ERR_CONFIG;
+    const int64_t nt_est = cdiv(kseg, 8) + (aligned ? 0 : 1);
+    // slices and per-lane depth
+    int S;
+    if (f->warp_split) {
+      S = f->warp_split;
+      if (S < 1 || S > W || W % S != 0) return GEMV_ERR_CONFIG;
+    } else {
+      // Slices of about 32 * 16 blocks (16 loads per lane in two rounds):
+      // on GB300 this balanced per-warp depth against the cost of the
+      // per-tile slice reduction best (k = 4096 -> 1, 7168/8192 -> 2,
+      // 14336/16384 -> 4 warps per row).
+      const int64_t q = (nt_est + 256) / 512;  // nt_est / 512, rounded
+      S = (int)pow2_floor(q < 1 ? 1 : q);
+      if (2 * S <= W && nt_est > 3 * S * 512 / 2) S *= 2;  // round up past 1.5x
+      if (S > W) S = W;
+      // Too few row tiles to occupy every CTA: split rows further while a
+      // slice keeps at least 4 loads per lane.
+      const int64_t resident_est = (int64_t)sm * cps_warps;
+      while (S < W && nt_est / (2 * S) >= 128 &&
+             cdiv(cdiv(n, NCLS), (int64_t)(W / S)) * NCLS < resident_est) {
+        S *= 2;
+      }
+    }
+    int R, U;
+    if (f->rows_per_warp || f->unroll) {
+      R = f->rows_per_warp ? f->rows_per_warp : 1;
+      U = f->unroll ? f->unroll : (R == 1 ? 8 : (R == 2 ? 4 : 2));
+      if (!valid_tiles_RU(R, U)) return GEMV_ERR_CONFIG;
+    } else {
+      const int64_t L = cdiv(nt_est, S);
+      if (S == 1 && L <= 64) {
+        R = 4; U = 2;
+      } else if (S == 1 && L <= 128) {
+        R = 2; U = 4;
+      } else if (L <= 128) {
+        R = 1; U = 4;
+      } else {
+        R = 1; U = 8;
+      }
+    }
+    // row tiles and grid
+    const int64_t RT = (int64_t)(W / S) * R;
+    const int64_t rows_per_class = cdiv(n, NCLS);
+    const int64_t groups = cdiv(rows_per_class, RT);  // tiles per class per segment
+    const int64_t as_elems = round_up(kseg + 24, 8);
+    const int64_t smem = as_elems * 2 + 2LL * W * R * 4;
+    if (smem > kMaxSmemPerCta) return GEMV_ERR_CONFIG;
+    int cps = cps_warps;
+    const int64_t cps_smem = kSmemPerSm / (smem + kSmemReservedPerCta);
+    if (cps_smem < cps) cps = (int)cps_smem;
+    if (cps < 1) return GEMV_ERR_CONFIG;
+    const int64_t resident = (int64_t)sm * cps;
+    // Few rows and long rows: split k across CTAs so that every SM works.
+    if (!f->grid_split && groups * NCLS * Sg < resident / 2) {
+      const int64_t more = resident / (groups * NCLS);
+      const int64_t max_by_k = cdiv(k, 256 * 8) > 1 ? cdiv(k, 256 * 8) : 1;
+      int64_t Sg2 = more < max_by_k ? more : max_by_k;
+      if (Sg2 > kMaxGridSplit) Sg2 = kMaxGridSplit;
+      if (Sg2 > Sg) {
+        Sg = Sg2;
+        kseg = round_up(cdiv(k, Sg), 8);
+        Sg = cdiv(k, kseg);
+      }
+    }
+    int64_t C;
+    if (f->ctas) {
+      C = (f->ctas / Sg) / NCLS * NCLS;
+    } else {
+      C = resident / Sg;
+      const int64_t need = groups * NCLS;  // CTAs that would have work
+      if (C > need) C = need;
+      C = C / NCLS * NCLS;
+    }
+    if (C < NCLS) C = NCLS;
+    if (C * Sg > INT32_MAX) return GEMV_ERR_CONFIG;
+
+    gemv_config c{};
+    c.variant = GEMV_VARIANT_TILES;
+    c.rows_per_warp = R;
+    c.unroll = U;
+    c.warps_per_cta = W;
+    c.warp_split = S;
+    c.grid_split = (int32_t)Sg;
+    c.row_blocks = (int32_t)C;
+    c.ctas = (int32_t)(C * Sg);
+    c.smem_bytes = (int32_t)(round_up(kseg + 24, 8) * 2 + 2LL * W * R * 4);
+    c.launches = Sg > 1 ? 2 : 1;
+    c.k_segment = kseg;
+    best = c;
+    have = true;
+    if (f->warps_per_cta || c.ctas >= sm) break;
+  }
+  if (!have) return GEMV_ERR_CONFIG;
+  *out = best;
+  return GEMV_OK;
+}
+
 // The planner.  Pure host arithmetic: no CUDA call.
 int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_config *f,
               gemv_config *out) {
@@ -126,7 +250,10 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
   gemv_config fz{};
   if (f == nullptr) f = &fz;
 
-  const int variant = f->variant ? f->variant : (aligned ? GEMV_VARIANT_ROWS : GEMV_VARIANT_ROWS_GENERAL);
+  const int auto_variant = (kAutoVariant == GEMV_VARIANT_ROWS && !aligned) ? GEMV_VARIANT_ROWS_GENERAL
+                                                                            : kAutoVariant;
+  const int variant = f->variant ? f->variant : auto_variant;
+  if (variant == GEMV_VARIANT_TILES) return plan_tiles(n, k, aligned, sm, f, out);
   if (variant != GEMV_VARIANT_ROWS && variant != GEMV_VARIANT_ROWS_GENERAL) return GEMV_ERR_CONFIG;
   if (variant == GEMV_VARIANT_ROWS && !aligned) return GEMV_ERR_CONFIG;
 
@@ -225,8 +352,12 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
   return GEMV_OK;
 }
 
-MainKernel lookup_main(int dtype, const gemv_config &c) {
+MainKernel lookup_main(int dtype, const gemv_config &c, bool aligned) {
   const int of = dtype >= 2 ? 1 : 0;
+  if (c.variant == GEMV_VARIANT_TILES) {
+    return (dtype & 1) ? tiles_kernel_bf16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll)
+                       : tiles_kernel_f16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll);
+  }
   return (dtype & 1) ? main_kernel_bf16(of, c.variant, c.rows_per_warp)
                      : main_kernel_f16(of, c.variant, c.rows_per_warp);
 }
@@ -320,6 +451,8 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
     return GEMV_OK;
   }
   const bool aligned = (((uintptr_t)B & 15u) == 0) && (k % 8 == 0);
+  const int overlap = forced ? forced->overlap : GEMV_OVERLAP_NONE;
+  if (overlap < GEMV_OVERLAP_NONE || overlap > GEMV_OVERLAP_PDL_PREFETCH_B) return GEMV_ERR_CONFIG;
 
   gemv_config cfg{};
   float *ws = nullptr;
@@ -330,7 +463,7 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
     if (!di.ok) return GEMV_ERR_DEVICE;
     const bool is_forced = forced != nullptr && (forced->variant || forced->rows_per_warp ||
                                                  forced->warps_per_cta || forced->warp_split ||
-                                                 forced->grid_split || forced->ctas);
+                                                 forced->grid_split || forced->ctas || forced->unroll);
     if (is_forced) {
       st = plan_impl(n, k, dtype, aligned, di.sm_count, forced, &cfg);
       if (st != GEMV_OK) return st;
@@ -346,7 +479,7 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
       }
     }
     if (cfg.smem_bytes > di.max_smem_optin) return GEMV_ERR_CONFIG;
-    mk = lookup_main(dtype, cfg);
+    mk = lookup_main(dtype, cfg, aligned);
     if (mk == nullptr) return GEMV_ERR_CONFIG;
     e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -369,18 +502,32 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
   p.sw = cfg.warp_split;
   p.nrb = cfg.row_blocks;
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
+  p.flags = (overlap == GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0;
 
-  mk<<<cfg.ctas, cfg.warps_per_cta * 32, cfg.smem_bytes, stream>>>(p);
-  e = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.ctas);
+  lc.blockDim = dim3((unsigned)(cfg.warps_per_cta * 32));
+  lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
+  lc.stream = stream;
+  lc.attrs = attr;
+  lc.numAttrs = overlap != GEMV_OVERLAP_NONE ? 1 : 0;
+  e = cudaLaunchKernelEx(&lc, mk, p);
   if (e != cudaSuccess) return cuda_fail(e);
   if (cfg.grid_split > 1) {
     ReduceKernel rk = lookup_reduce(dtype);
     int64_t blocks = cdiv(n, kReduceThreads);
     if (blocks > 65535) blocks = 65535;
-    rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split);
-    e = cudaGetLastError();
+    lc.gridDim = dim3((unsigned)blocks);
+    lc.blockDim = dim3(kReduceThreads);
+    lc.dynamicSmemBytes = 0;
+    const float *wsc = ws;
+    e = cudaLaunchKernelEx(&lc, rk, wsc, c, n, (int32_t)cfg.grid_split);
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  cfg.overlap = overlap;
   t_last = cfg;
   t_has_last = true;
   return GEMV_OK;
@@ -431,7 +578,7 @@ extern "C" int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cu
     if (st != GEMV_OK) return st;
     g_cache.emplace(key, cfg);
   }
-  MainKernel mk = lookup_main(dtype, cfg);
+  MainKernel mk = lookup_main(dtype, cfg, aligned);
   if (mk == nullptr) return GEMV_ERR_CONFIG;
   cudaError_t e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
   if (e != cudaSuccess) return cuda_fail(e);

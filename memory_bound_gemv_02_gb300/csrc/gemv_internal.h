@@ -20,6 +20,8 @@ struct Params {
   int32_t sw;         // warp split (warps per row inside a CTA)
   int32_t nrb;        // row blocks = gridDim.x / sg
   int32_t as_elems;   // staged a elements per CTA (multiple of 8, >= kseg + 24)
+  int32_t flags;      // kFlagPrefetchB: read the first B tile before waiting on the predecessor
+  // Tiles kernel: sw = S (warps per row, slices), nrb = C (CTAs per k-segment).
 };
 
 typedef void (*MainKernel)(Params);
@@ -31,6 +33,10 @@ typedef void (*ProbeKernel)(const uint4 *, int64_t, uint32_t *);
 // Returns nullptr for a combination that is not instantiated.
 MainKernel main_kernel_f16(int out_f32, int variant, int R);
 MainKernel main_kernel_bf16(int out_f32, int variant, int R);
+// Tiles kernel: aligned = 1 for the single-class fast path; (R, U) in
+// {(1,8), (1,4), (2,4), (4,2)}.
+MainKernel tiles_kernel_f16(int out_f32, int aligned, int R, int U);
+MainKernel tiles_kernel_bf16(int out_f32, int aligned, int R, int U);
 ReduceKernel reduce_kernel_f16(int out_f32);
 ReduceKernel reduce_kernel_bf16(int out_f32);
 ProbeKernel probe_kernel();
@@ -39,5 +45,6 @@ ProbeKernel probe_kernel();
 inline int unroll_for_rows(int R) { return R == 1 ? 8 : (R == 2 ? 4 : 2); }
 
 constexpr int kMaxThreads = 512;  // launch bound of the main kernel
+constexpr int kFlagPrefetchB = 1;
 
 }  // namespace gemvk

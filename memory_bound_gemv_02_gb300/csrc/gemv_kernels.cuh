@@ -68,6 +68,14 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
 
 __device__ __forceinline__ uint4 zero4() { return make_uint4(0u, 0u, 0u, 0u); }
 
+// Programmatic dependent launch.  allow_dependents(): the next kernel on the
+// stream (if launched with the programmatic-serialization attribute) may be
+// scheduled once every CTA of this grid has executed it or exited.
+// wait_for_predecessor(): blocks until the preceding grid has completed and
+// its memory is visible; a no-op when this grid was launched normally.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------ arithmetic --
 
 // Widen a 16-byte vector of a (8 elements) to fp32.
@@ -301,6 +309,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_rows_kernel(Params p) {
   const int64_t j0 = (int64_t)gs * p.kseg;
   const int64_t len = (p.k - j0 < p.kseg) ? (p.k - j0) : p.kseg;
 
+  allow_dependents();
+  wait_for_predecessor();
   stage_a(p, as4, j0, len);
   __syncthreads();
 
@@ -350,6 +360,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_rows_kernel(Params p) {
 // order) of ws[s * n + row], rounded once to the output type.
 template <class T, bool OUT_F32>
 __global__ void __launch_bounds__(256) gemv_splitk_reduce_kernel(const float *ws, void *c, int64_t n, int32_t sg) {
+  allow_dependents();
+  wait_for_predecessor();  // the partials come from the kernel before
   for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < n;
        row += (int64_t)gridDim.x * blockDim.x) {
     float v = 0.f;

@@ -1,0 +1,231 @@
+// "Tiles" GEMV kernel for sm_103a: c = B @ a, B (n, k) row-major, fp16/bf16
+// in, fp32 accumulation (TileLang Case Studies, Case B).
+//
+// Differences from the row-per-warp kernel, both measured on GB300:
+//
+//  * Dense access order.  A CTA works on tiles of RT consecutive rows of its
+//    row class, and tile g of every CTA lies next to tile g of the others,
+//    so at any moment the whole GPU streams one narrow, contiguous window of
+//    B (the order a grid-stride copy uses), instead of thousands of
+//    unrelated row streams spread over the matrix.
+//  * One code path for any alignment.  The rows of B start at element
+//    offset (base + i*k) mod 8 inside a 16-byte block, which depends only on
+//    i mod 8.  CTAs are assigned one residue class of rows each, so every
+//    row a CTA reads has the same offset `off`: the CTA stages its k-segment
+//    of a shifted by `off` once, and row blocks then line up with staged
+//    16-byte vectors of a.  The only extra work for k % 8 != 0 is masking
+//    the first and last block of each row (elements of neighbouring rows).
+//  * Rows are split into S slices of L blocks (one warp per slice, each lane
+//    streaming up to U 16-byte blocks, R rows side by side for short rows);
+//    the S slice sums of a row are combined in shared memory in slice order
+//    after a named barrier among the S warps of that row team (double-
+//    buffered, so one barrier per tile suffices).
+#pragma once
+
+#include "gemv_kernels.cuh"
+
+namespace gemvk {
+
+__device__ __forceinline__ void team_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Stage columns [j0, j0 + len) of a, shifted right by `off` elements:
+// as[x] = a[j0 + x - off] for off <= x < off + len, 0 for other x < as_elems.
+// Block t of a row that starts at offset `off` then multiplies as4[t].
+__device__ __forceinline__ void stage_a_shifted(const Params &p, uint4 *as4, int64_t j0, int64_t len, int off) {
+  const int nvec = p.as_elems >> 3;
+  const uint16_t *aj = p.a + j0;
+  const bool vec_ok = off == 0 && (reinterpret_cast<uintptr_t>(aj) & 15u) == 0;
+  for (int q = threadIdx.x; q < nvec; q += blockDim.x) {
+    const int64_t jb = 8 * (int64_t)q - off;  // segment column of element 0 of this vector
+    uint4 v;
+    if (vec_ok && jb + 8 <= len) {
+      v = __ldg(reinterpret_cast<const uint4 *>(aj + jb));
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int64_t j_lo = jb + 2 * h, j_hi = jb + 2 * h + 1;
+        const uint32_t lo = (j_lo >= 0 && j_lo < len) ? (uint32_t)__ldg(aj + j_lo) : 0u;
+        const uint32_t hi = (j_hi >= 0 && j_hi < len) ? (uint32_t)__ldg(aj + j_hi) : 0u;
+        w[h] = lo | (hi << 16);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    as4[q] = v;
+  }
+}
+
+// Issue this lane's loads of one step of a row slice: blocks t + 32u
+// (u < U) of the R rows, predicated on t + 32u < t1 and the row being real.
+template <int U, int R>
+__device__ __forceinline__ void tile_issue(const uint4 *bal, const int64_t (&g0)[R], const bool (&valid)[R],
+                                           int t, int t1, uint4 (&bv)[U][R]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int tt = t + 32 * u;
+#pragma unroll
+    for (int r = 0; r < R; ++r) bv[u][r] = (tt < t1 && valid[r]) ? ldg_stream(bal + g0[r] + tt) : zero4();
+  }
+}
+
+// Multiply-accumulate one step's blocks with the staged (pre-shifted) a.
+// Unaligned rows: the first and last block of a row carry elements of the
+// neighbouring rows, which are zeroed first.
+template <class T, int U, int R, int NA, bool ALIGNED>
+__device__ __forceinline__ void tile_consume(const uint4 *as4, const uint4 (&bv)[U][R], int t, int t1, int nt,
+                                             int off, int last_hi, float (&acc)[R][NA]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int tt = t + 32 * u;
+    if (tt < t1) {
+      float af[8];
+      widen8<T>(as4[tt], af);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        uint4 b = bv[u][r];
+        if constexpr (!ALIGNED) {
+          if (tt == 0 || tt == nt - 1) b = keep_range(b, tt == 0 ? off : 0, tt == nt - 1 ? last_hi : 8);
+        }
+        fma8<T, NA>(b, af, acc[r]);
+      }
+    }
+  }
+}
+
+// Grid: blockIdx.x = c * sg + gs, c in [0, C) with C = p.nrb.  ALIGNED
+// (k % 8 == 0 and B 16-byte aligned) uses one row class; otherwise 8 classes
+// (C must be a multiple of 8), CTA c serving class c % 8.
+template <class T, bool OUT_F32, int U, int R, bool ALIGNED>
+__global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
+  extern __shared__ __align__(16) uint4 smem4[];
+  uint4 *as4 = smem4;
+  float *ps = reinterpret_cast<float *>(smem4 + (p.as_elems >> 3));  // [2][W * R]
+  constexpr int NA = (R == 1) ? 4 : (R == 2 ? 2 : 1);
+
+  const int W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gs = blockIdx.x % p.sg;
+  const int c = blockIdx.x / p.sg;
+  constexpr int NCLS = ALIGNED ? 1 : 8;
+  const int cls = c % NCLS, cq = c / NCLS, Cq = p.nrb / NCLS;
+  const int64_t j0 = (int64_t)gs * p.kseg;
+  const int64_t len = (p.k - j0 < p.kseg) ? (p.k - j0) : p.kseg;
+  // rows of this class: i = NCLS * j + cls, 0 <= j < nr
+  const int64_t nr = (p.n > cls) ? (p.n - cls + NCLS - 1) / NCLS : 0;
+  const int off = ALIGNED ? 0 : (int)(((int64_t)p.base_off + j0 + (int64_t)cls * (p.k & 7)) & 7);
+  const int nt = (int)((off + len + 7) >> 3);
+  const int last_hi = (int)(len + off - 8 * (int64_t)(nt - 1));
+
+  const uint4 *bal = reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p.B) & ~(uintptr_t)15);
+  const int S = p.sw, slots = W / S, slot = warp / S, s = warp % S;
+  const int RT = slots * R;  // rows of the class per tile
+  const int L = (nt + S - 1) / S;
+  const int t0 = s * L < nt ? s * L : nt;
+  const int t1 = t0 + L < nt ? t0 + L : nt;
+  const int64_t ngroups = (nr + RT - 1) / RT;
+
+  auto rows_of = [&](int64_t g, int64_t (&g0)[R], bool (&valid)[R]) {
+    const int64_t jb = g * RT + (int64_t)slot * R;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      valid[r] = (jb + r) < nr;
+      const int64_t i = NCLS * (jb + r) + cls;
+      g0[r] = valid[r] ? (((int64_t)p.base_off + i * p.k + j0) >> 3) : 0;
+    }
+  };
+
+  // The first tile's first loads go out before a is staged, so the B
+  // stream starts at once and the staging latency hides under it.  Under a
+  // programmatic dependent launch with kFlagPrefetchB they even go out
+  // before the preceding kernel has finished (B is then promised read-only);
+  // a and c are touched only after wait_for_predecessor().
+  allow_dependents();
+  const bool early = (p.flags & kFlagPrefetchB) != 0;
+  if (!early) wait_for_predecessor();
+  uint4 bv[U][R];
+  bool prefetched = false;
+  if (cq < ngroups) {
+    int64_t g0[R];
+    bool valid[R];
+    rows_of(cq, g0, valid);
+    tile_issue<U, R>(bal, g0, valid, t0 + lane, t1, bv);
+    prefetched = true;
+  }
+  if (early) wait_for_predecessor();
+  stage_a_shifted(p, as4, j0, len, off);
+  __syncthreads();
+
+  int buf = 0;
+  for (int64_t g = cq; g < ngroups; g += Cq) {
+    int64_t g0[R];
+    bool valid[R];
+    rows_of(g, g0, valid);
+    float acc[R][NA];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int q = 0; q < NA; ++q) acc[r][q] = 0.f;
+    }
+    for (int t = t0 + lane; t < t1; t += 32 * U) {
+      if (!prefetched) tile_issue<U, R>(bal, g0, valid, t, t1, bv);
+      prefetched = false;
+      tile_consume<T, U, R, NA, ALIGNED>(as4, bv, t, t1, nt, off, last_hi, acc);
+    }
+    prefetched = false;
+    float v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float x = acc[r][0];
+#pragma unroll
+      for (int q = 1; q < NA; ++q) x += acc[r][q];
+      v[r] = warp_sum(x);
+    }
+    const int64_t jb = g * RT + (int64_t)slot * R;
+    if (S == 1) {
+      if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (valid[r]) store_out<T, OUT_F32>(p, gs, NCLS * (jb + r) + cls, v[r]);
+      }
+    } else {
+      float *pb = ps + buf * (W * R);
+      if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) pb[(slot * R + r) * S + s] = v[r];
+      }
+      team_barrier(1 + slot, S * 32);
+      if (s == 0 && lane < R) {
+        const int64_t j = jb + lane;
+        if (j < nr) {
+          float sum = 0.f;
+          for (int s2 = 0; s2 < S; ++s2) sum += pb[(slot * R + lane) * S + s2];
+          store_out<T, OUT_F32>(p, gs, NCLS * j + cls, sum);
+        }
+      }
+      buf ^= 1;
+    }
+  }
+}
+
+}  // namespace gemvk
+
+// Instantiations of the tiles kernel for one input type: (U, R) in
+// {(8,1), (4,1), (4,2), (2,4)}, aligned or not, output same type or fp32.
+#define GEMV_TILES_CASES(T, OF, AL)                                     \
+  if (U == 8 && R == 1) return gemv_tiles_kernel<T, OF, 8, 1, AL>;      \
+  if (U == 4 && R == 1) return gemv_tiles_kernel<T, OF, 4, 1, AL>;      \
+  if (U == 4 && R == 2) return gemv_tiles_kernel<T, OF, 4, 2, AL>;      \
+  if (U == 2 && R == 4) return gemv_tiles_kernel<T, OF, 2, 4, AL>;
+
+#define GEMV_DEFINE_TILES_TABLE(T, SUFFIX)                                                  \
+  namespace gemvk {                                                                         \
+  MainKernel tiles_kernel_##SUFFIX(int out_f32, int aligned, int R, int U) {                \
+    if (out_f32) {                                                                          \
+      if (aligned) { GEMV_TILES_CASES(T, true, true) } else { GEMV_TILES_CASES(T, true, false) } \
+    } else {                                                                                \
+      if (aligned) { GEMV_TILES_CASES(T, false, true) } else { GEMV_TILES_CASES(T, false, false) } \
+    }                                                                                       \
+    return nullptr;                                                                         \
+  }                                                                                         \
+  }

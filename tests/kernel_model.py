@@ -24,6 +24,8 @@ def _row_range(rbk, n, nrb):
 
 def replay(n, k, cfg, base_off=0):
     """Return a dict of findings; raises AssertionError on any violation."""
+    if cfg["variant"] == 3:
+        return replay_tiles(n, k, cfg, base_off)
     W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
     nrb, kseg, variant, ctas = cfg["row_blocks"], cfg["k_segment"], cfg["variant"], cfg["ctas"]
     assert ctas == nrb * Sg and W % Sw == 0
@@ -98,6 +100,86 @@ def replay(n, k, cfg, base_off=0):
                 idx = gs * n + row
                 assert 0 <= idx < Sg * n
                 ws_rows.add(idx)
+    assert (cover == 1).all(), f"coverage wrong: min {cover.min()} max {cover.max()}"
+    if Sg > 1:
+        assert len(ws_rows) == Sg * n
+    return {"ctas": ctas}
+
+
+def replay_tiles(n, k, cfg, base_off=0):
+    """The same checks for ``gemv_tiles_kernel``."""
+    W, R, S, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
+    C, kseg, U, ctas = cfg["row_blocks"], cfg["k_segment"], cfg["unroll"], cfg["ctas"]
+    aligned = base_off == 0 and k % 8 == 0
+    NCLS = 1 if aligned else 8
+    assert ctas == C * Sg and W % S == 0 and C % NCLS == 0 and C >= NCLS
+    assert (R, U) in ((1, 8), (1, 4), (2, 4), (4, 2))
+    as_elems = -(-(kseg + 24) // 8) * 8
+    assert cfg["smem_bytes"] == as_elems * 2 + 2 * W * R * 4
+    slots = W // S
+    if S > 1:
+        assert 1 + slots - 1 <= 15  # named barrier ids 1..slots
+    cover = np.zeros((n, k), dtype=np.int32)
+    nblocks = -(-(base_off + n * k) // 8)
+    ws_rows = set()
+    Cq = C // NCLS
+    for cta in range(ctas):
+        gs, c = cta % Sg, cta // Sg
+        cls, cq = c % NCLS, c // NCLS
+        j0 = gs * kseg
+        seglen = min(k - j0, kseg)
+        assert seglen >= 1
+        nr = (n - cls + NCLS - 1) // NCLS if n > cls else 0
+        off = 0 if aligned else (base_off + j0 + cls * (k & 7)) & 7
+        nt = (off + seglen + 7) >> 3
+        last_hi = seglen + off - 8 * (nt - 1)
+        assert 1 <= last_hi <= 8
+        assert nt <= as_elems // 8
+        RT = slots * R
+        L = -(-nt // S)
+        ngroups = -(-nr // RT)
+        stage_x = np.arange(8 * nt)
+        stage_col = stage_x - off  # segment column held by staged element x
+        for g in range(cq, ngroups, Cq):
+            for warp in range(W):
+                slot, s = divmod(warp, S)
+                jb = g * RT + slot * R
+                t0 = min(s * L, nt)
+                t1 = min(t0 + L, nt)
+                if S > 1:
+                    for r in range(R):
+                        assert 0 <= (slot * R + r) * S + s < W * R
+                for r in range(R):
+                    j = jb + r
+                    if j >= nr:
+                        continue
+                    i = NCLS * j + cls
+                    assert i < n
+                    e0 = base_off + i * k + j0
+                    assert (e0 & 7) == off, "row offset differs inside a CTA"
+                    g0 = e0 >> 3
+                    if t1 <= t0:
+                        continue
+                    t = np.arange(t0, t1)
+                    blk = g0 + t
+                    assert blk.min() >= 0 and blk.max() < nblocks
+                    p = np.arange(8)[None, :]
+                    tt = t[:, None]
+                    if aligned:
+                        valid = np.ones((t.size, 8), bool)
+                    else:
+                        valid = ((tt > 0) | (p >= off)) & ((tt < nt - 1) | (p < last_hi))
+                    elem = 8 * blk[:, None] + p - base_off
+                    col_B = elem - i * k - j0
+                    col_stage = stage_col[8 * tt + p]
+                    assert (col_B[valid] == col_stage[valid]).all()
+                    assert (col_B[valid] >= 0).all() and (col_B[valid] < seglen).all()
+                    # masked-off staged entries must be zero-filled (outside the segment)
+                    if aligned:
+                        assert ((col_stage >= 0) & (col_stage < seglen)).all()
+                    np.add.at(cover[i], j0 + col_B[valid], 1)
+                    if Sg > 1:
+                        ws_rows.add(gs * n + i)
     assert (cover == 1).all(), f"coverage wrong: min {cover.min()} max {cover.max()}"
     if Sg > 1:
         assert len(ws_rows) == Sg * n

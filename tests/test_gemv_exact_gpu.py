@@ -24,7 +24,10 @@ from memory_bound_gemv_02_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 CONFIGS = [None, {"variant": 2}, {"rows_per_warp": 4}, {"warps_per_cta": 4, "warp_split": 4},
-           {"grid_split": 3}, {"grid_split": 2, "warp_split": 8}, {"ctas": 3}]
+           {"grid_split": 3}, {"grid_split": 2, "warp_split": 8}, {"ctas": 3},
+           {"variant": 3}, {"variant": 3, "warp_split": 4}, {"variant": 3, "rows_per_warp": 4, "unroll": 2},
+           {"variant": 3, "rows_per_warp": 2, "unroll": 4, "warps_per_cta": 8},
+           {"variant": 3, "grid_split": 3, "warp_split": 2}, {"variant": 3, "ctas": 8}]
 
 
 def _run(B, a, out_fp32=False, config=None, c=None):
@@ -88,11 +91,13 @@ TAIL_K = [1, 2, 5, 8, 9, 15, 16, 17, 31, 33, 255, 256, 257, 4099]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_ragged_tails_bit_exact(cuda_dev, dtype):
+@pytest.mark.parametrize("variant", [None, 3])
+def test_ragged_tails_bit_exact(cuda_dev, dtype, variant):
+    cfg = {"variant": variant} if variant else None
     for n, k in itertools.product(TAIL_N, TAIL_K):
         B, a = inputs.make_int_inputs(n, k, dtype, seed=7 * n + k, device=cuda_dev)
-        c = _run(B, a, False)
-        assert exact_bits_match(c, B, a, False), (n, k)
+        c = _run(B, a, False, cfg)
+        assert exact_bits_match(c, B, a, False), (n, k, cfg)
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
@@ -110,8 +115,10 @@ def test_offset_views_take_the_general_path(cuda_dev, dtype, b_off, a_off):
         av.copy_(ai)
         c = _run(Bv, av, False)
         if b_off % 8 or k % 8:
-            assert g.gemv_last_config()["variant"] == g.GEMV_VARIANT_ROWS_GENERAL
+            assert g.gemv_last_config()["variant"] in (g.GEMV_VARIANT_ROWS_GENERAL, g.GEMV_VARIANT_TILES)
         assert exact_bits_match(c, Bi, ai, False), (n, k, b_off, a_off)
+        c = _run(Bv, av, False, {"variant": 3})
+        assert exact_bits_match(c, Bi, ai, False), (n, k, b_off, a_off, "tiles")
         Bu, au = inputs.make_inputs(n, k, dtype, "uniform", 9, cuda_dev)
         Bv.copy_(Bu)
         av.copy_(au)
@@ -187,7 +194,8 @@ def test_error_paths_launch_nothing(cuda_dev):
 def test_determinism_repeated_calls(cuda_dev):
     """Fixed-order reductions: 200 calls give bitwise-identical results (a
     race in the cross-warp or split-K combination would show up here)."""
-    for cfg in (None, {"warp_split": 8, "warps_per_cta": 16}, {"grid_split": 4}):
+    for cfg in (None, {"warp_split": 8, "warps_per_cta": 16}, {"grid_split": 4},
+                {"variant": 3, "warp_split": 4}, {"variant": 3, "grid_split": 2, "warp_split": 8}):
         B, a = inputs.make_inputs(3001, 5000, "f16", "normal", 2, cuda_dev, b_sigma=0.5)
         first = _run(B, a, True, cfg).clone()
         c = torch.empty_like(first)
@@ -253,3 +261,68 @@ def test_host_overhead_per_call(cuda_dev):
         torch.cuda.synchronize()
     med = float(np.median(per))
     assert med < 10e-6, f"host time per call {med * 1e6:.2f} us"
+
+
+@pytest.mark.parametrize("overlap", [1, 2])
+@pytest.mark.parametrize("variant", [None, 3])
+def test_overlap_respects_dependencies(cuda_dev, overlap, variant):
+    """Programmatic dependent launch: each call still sees the memory of the
+    kernels before it.  A chain x_{m+1} = B @ x_m (c of one call is a of the
+    next), torch kernels rewriting a between calls, and two calls writing the
+    same c with different B."""
+    cfg = {"overlap": overlap}
+    if variant:
+        cfg["variant"] = variant
+    n = 2048
+    B, x0 = inputs.make_int_inputs(n, n, "bf16", seed=3, device=cuda_dev, lo=-1, hi=1)
+    B = B * (1.0 / 64)  # keeps the chain's values inside bf16 range, exactly
+    xs = [x0]
+    for _ in range(12):
+        xs.append(g.gemv_ex(B, xs[-1], config=cfg))
+    torch.cuda.synchronize()
+    for m in range(12):
+        check_against_oracle(xs[m + 1], B, xs[m], False, label=f"chain step {m} overlap {overlap}")
+    # a rewritten by a torch kernel right before each call
+    a = torch.empty(n, dtype=torch.bfloat16, device=cuda_dev)
+    outs = []
+    for m in range(6):
+        a.copy_(xs[m])
+        outs.append(g.gemv_ex(B, a, config=cfg))
+    torch.cuda.synchronize()
+    for m in range(6):
+        check_against_oracle(outs[m], B, xs[m], False, label=f"a rewritten {m}")
+    # same c written by consecutive calls: the last one wins
+    B2 = B * 2
+    c = torch.empty(n, dtype=torch.bfloat16, device=cuda_dev)
+    for _ in range(5):
+        g.gemv_ex(B, xs[0], c=c, config=cfg)
+        g.gemv_ex(B2, xs[0], c=c, config=cfg)
+    check_against_oracle(c, B2, xs[0], False, label="WAW on c")
+
+
+@pytest.mark.parametrize("variant", [None, 3])
+def test_overlap_pdl_sees_rewritten_B(cuda_dev, variant):
+    """GEMV_OVERLAP_PDL (without the B prefetch) also orders B: a kernel that
+    rewrites B right before the call is waited for."""
+    cfg = {"overlap": 1}
+    if variant:
+        cfg["variant"] = variant
+    B, a = inputs.make_inputs(3000, 4104, "f16", "uniform", 6, cuda_dev)
+    Bw = torch.empty_like(B)
+    for m in range(4):
+        Bw.copy_(B * (m + 1))
+        c = g.gemv_ex(Bw, a, config=cfg)
+        check_against_oracle(c, B * (m + 1), a, False, label=f"B rewritten {m}")
+
+
+def test_overlap_uses_cached_plan(cuda_dev):
+    B, a = inputs.make_inputs(777, 5000, "bf16", "uniform", 7, cuda_dev)
+    g.gemv(B, a)
+    base = g.gemv_last_config()
+    g.gemv_ex(B, a, config={"overlap": 2})
+    got = g.gemv_last_config()
+    assert got["overlap"] == 2
+    assert {k: v for k, v in got.items() if k != "overlap"} == {k: v for k, v in base.items() if k != "overlap"}
+    with pytest.raises(g.GemvError) as ei:
+        g.gemv_ex(B, a, config={"overlap": 3})
+    assert ei.value.status == g.GEMV_ERR_CONFIG

@@ -107,6 +107,8 @@ FORCED = [
     {"warps_per_cta": 16, "warp_split": 4},
     {"grid_split": 2}, {"grid_split": 5, "warp_split": 2},
     {"ctas": 1}, {"ctas": 37, "rows_per_warp": 2},
+    {"variant": 3}, {"variant": 3, "warp_split": 8}, {"variant": 3, "warp_split": 2, "warps_per_cta": 4},
+    {"variant": 3, "rows_per_warp": 2, "unroll": 4}, {"variant": 3, "grid_split": 4},
 ]
 
 
@@ -118,7 +120,7 @@ def test_forced_configs_parity(cuda_dev, cfg, dtype):
         c = _run(B, a, out_fp32, cfg)
         used = g.gemv_last_config()
         for key, v in cfg.items():
-            if key != "ctas":
+            if key not in ("ctas", "grid_split"):
                 assert used[key] == v
         check_against_oracle(c, B, a, out_fp32, label=f"{cfg} {dtype} f32out={out_fp32}")
 
@@ -132,9 +134,20 @@ def test_errors_differ_across_variants(cuda_dev):
     c_ref, _ = h.oracle_for(B, a)
     maxerrs = set()
     for cfg in [None, {"rows_per_warp": 2}, {"warp_split": 4, "warps_per_cta": 16}, {"grid_split": 3},
-                {"variant": 2}]:
+                {"variant": 2}, {"variant": 3}]:
         c = _run(B, a, True, cfg)
         torch.cuda.synchronize()
         err = abs(h.gpu_values(c) - c_ref).max()
         maxerrs.add(float(err))
     assert len(maxerrs) >= 2
+
+
+@pytest.mark.parametrize("n,k,dtype", [(7168, 16384, "f16"), (18432, 7168, "bf16"), (65536, 7169, "f16"),
+                                       (18433, 7169, "bf16"), (4099, 1000, "f16"), (1024, 16384, "bf16"),
+                                       (256, 512, "f16")])
+def test_tiles_variant_workloads(cuda_dev, n, k, dtype):
+    B, a = inputs.make_inputs(n, k, dtype, "uniform", 1, cuda_dev)
+    for out_fp32 in (False, True):
+        c = _run(B, a, out_fp32, {"variant": 3})
+        check_against_oracle(c, B, a, out_fp32, rows=sample_rows(n, 128),
+                             label=f"tiles {n}x{k} {dtype} f32out={out_fp32}")

@@ -26,9 +26,7 @@ def test_plan_invariants(gemv_lib, n, k, dtype, aligned, sm):
     cfg = gemv_lib.gemv_plan(n, k, dtype, aligned, sm)
     W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
     assert W in (4, 8, 16) and R in (1, 2, 4) and W % Sw == 0
-    assert cfg["variant"] == (1 if aligned and k % 8 == 0 else 2)
-    if cfg["variant"] == 2:
-        assert R == 1
+    assert cfg["variant"] == 3
     kseg = cfg["k_segment"]
     assert Sg * kseg >= k and (Sg - 1) * kseg < k
     if Sg > 1:
@@ -38,12 +36,14 @@ def test_plan_invariants(gemv_lib, n, k, dtype, aligned, sm):
     assert cfg["launches"] == (2 if Sg > 1 else 1)
     # persistent grid: never more CTAs than can be resident at once
     cps = min(32 // W, 233472 // (cfg["smem_bytes"] + 1024))
-    assert cfg["ctas"] <= max(sm * cps, Sg)
+    assert cfg["ctas"] <= max(sm * cps, Sg * 8)
 
 
 def test_plan_shapes_of_interest(gemv_lib):
     big = gemv_lib.gemv_plan(7168, 16384, 0, True, SM)
-    assert big["grid_split"] == 1 and big["warp_split"] == 1 and big["variant"] == 1
+    assert big["grid_split"] == 1 and big["warp_split"] == 4 and big["variant"] == 3
+    assert gemv_lib.gemv_plan(18432, 7168, 1, True, SM)["warp_split"] == 2
+    assert gemv_lib.gemv_plan(65536, 4096, 1, True, SM)["warp_split"] == 1
     tiny_n = gemv_lib.gemv_plan(16, 16384, 0, True, SM)
     assert tiny_n["warp_split"] * tiny_n["grid_split"] > 1  # rows are split to fill the GPU
     huge_k = gemv_lib.gemv_plan(2, 2 ** 20, 1, True, SM)
@@ -51,9 +51,11 @@ def test_plan_shapes_of_interest(gemv_lib):
 
 
 @pytest.mark.parametrize("cfg", [
-    {"variant": 1, "rows_per_warp": 4}, {"warps_per_cta": 4, "warp_split": 4},
-    {"grid_split": 3}, {"warps_per_cta": 8, "warp_split": 2, "grid_split": 2},
-    {"ctas": 7}, {"ctas": 1}, {"warps_per_cta": 16, "warp_split": 16},
+    {"variant": 1, "rows_per_warp": 4}, {"variant": 1, "warps_per_cta": 4, "warp_split": 4},
+    {"variant": 1, "grid_split": 3}, {"variant": 1, "warps_per_cta": 8, "warp_split": 2, "grid_split": 2},
+    {"variant": 1, "ctas": 7}, {"variant": 1, "ctas": 1}, {"variant": 1, "warps_per_cta": 16, "warp_split": 16},
+    {"warps_per_cta": 4, "warp_split": 4}, {"grid_split": 3}, {"warps_per_cta": 8, "warp_split": 2, "grid_split": 2},
+    {"ctas": 16}, {"warps_per_cta": 16, "warp_split": 16}, {"rows_per_warp": 2, "unroll": 4},
 ])
 def test_forced_configs_are_honoured(gemv_lib, cfg):
     out = gemv_lib.gemv_plan(1000, 4096, 0, True, SM, config=cfg)
@@ -65,8 +67,8 @@ def test_forced_configs_are_honoured(gemv_lib, cfg):
 
 
 @pytest.mark.parametrize("cfg", [
-    {"variant": 3}, {"rows_per_warp": 3}, {"warps_per_cta": 12}, {"warps_per_cta": 8, "warp_split": 3},
-    {"grid_split": 65}, {"variant": 2, "rows_per_warp": 2},
+    {"variant": 4}, {"rows_per_warp": 3}, {"warps_per_cta": 12}, {"warps_per_cta": 8, "warp_split": 3},
+    {"grid_split": 65}, {"variant": 2, "rows_per_warp": 2}, {"rows_per_warp": 2, "unroll": 8},
 ])
 def test_invalid_forced_configs_rejected(gemv_lib, cfg):
     with pytest.raises(gemv_lib.GemvError) as ei:
@@ -94,7 +96,7 @@ SMALL = [(1, 1), (1, 8), (2, 7), (3, 9), (5, 17), (13, 31), (17, 64), (33, 100),
                                     {"ctas": 3}, {"warps_per_cta": 16, "warp_split": 16}])
 def test_general_variant_index_replay(gemv_lib, n, k, base_off, forced):
     try:
-        cfg = gemv_lib.gemv_plan(n, k, 0, False, SM, config=forced)
+        cfg = gemv_lib.gemv_plan(n, k, 0, False, SM, config={**(forced or {}), "variant": 2})
     except gemv_lib.GemvError:
         pytest.skip("configuration not valid for this shape")
     assert cfg["variant"] == 2
@@ -109,7 +111,7 @@ def test_general_variant_index_replay(gemv_lib, n, k, base_off, forced):
                                     {"warps_per_cta": 16, "warp_split": 8, "grid_split": 2}])
 def test_aligned_variant_index_replay(gemv_lib, n, k, forced):
     try:
-        cfg = gemv_lib.gemv_plan(n, k, 1, True, SM, config=forced)
+        cfg = gemv_lib.gemv_plan(n, k, 1, True, SM, config={**(forced or {}), "variant": 1})
     except gemv_lib.GemvError:
         pytest.skip("configuration not valid for this shape")
     assert cfg["variant"] == 1
@@ -121,3 +123,46 @@ def test_aligned_variant_index_replay(gemv_lib, n, k, forced):
 def test_planner_choice_replay_medium(gemv_lib, n, k, aligned):
     cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM)
     kernel_model.replay(n, k, cfg, base_off=0 if aligned else 3)
+
+
+# ------------------------------------------------------------ tiles variant --
+
+TILES_FORCED = [None, {"warp_split": 2}, {"warp_split": 4, "warps_per_cta": 8},
+                {"rows_per_warp": 2, "unroll": 4}, {"rows_per_warp": 4, "unroll": 2},
+                {"rows_per_warp": 1, "unroll": 4}, {"grid_split": 3}, {"ctas": 8},
+                {"warps_per_cta": 16, "warp_split": 16}, {"warps_per_cta": 4, "warp_split": 2, "grid_split": 2}]
+
+
+@pytest.mark.parametrize("n,k", SMALL + [(64, 512), (33, 1000), (300, 24), (2, 4096), (1, 2049)])
+@pytest.mark.parametrize("base_off", [0, 1, 6])
+@pytest.mark.parametrize("forced", TILES_FORCED)
+def test_tiles_index_replay(gemv_lib, n, k, base_off, forced):
+    cfg_in = dict(forced or {})
+    cfg_in["variant"] = 3
+    aligned = base_off == 0
+    try:
+        cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config=cfg_in)
+    except gemv_lib.GemvError:
+        pytest.skip("configuration not valid for this shape")
+    kernel_model.replay(n, k, cfg, base_off=base_off)
+
+
+@pytest.mark.parametrize("n,k", WORKLOADS)
+@pytest.mark.parametrize("aligned", [True, False])
+def test_tiles_plan_invariants(gemv_lib, n, k, aligned):
+    cfg = gemv_lib.gemv_plan(n, k, 1, aligned, SM, config={"variant": 3})
+    W, S, C, Sg = cfg["warps_per_cta"], cfg["warp_split"], cfg["row_blocks"], cfg["grid_split"]
+    ncls = 1 if aligned and k % 8 == 0 else 8
+    assert W % S == 0 and C % ncls == 0 and C >= ncls and cfg["ctas"] == C * Sg
+    assert Sg * cfg["k_segment"] >= k and (Sg - 1) * cfg["k_segment"] < k
+    assert cfg["smem_bytes"] <= MAX_SMEM
+    nt = -(-cfg["k_segment"] // 8) + (0 if ncls == 1 else 1)
+    # at most 8 loads per lane per row slice, unless the row is too long for 16 warps
+    assert -(-nt // S) <= 32 * cfg["unroll"] * 4
+
+
+@pytest.mark.parametrize("n,k,aligned", [(256, 512, True), (1024, 1000, True), (130, 7169, False),
+                                         (77, 4099, False), (1000, 600, False)])
+def test_tiles_planner_choice_replay_medium(gemv_lib, n, k, aligned):
+    cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 3})
+    kernel_model.replay(n, k, cfg, base_off=0 if aligned else 5)
