@@ -54,7 +54,8 @@ enum {
   GEMV_ERR_CUDA = -5,    /* a CUDA call or launch failed; see gemv_last_cuda_error() */
   GEMV_ERR_CONFIG = -6,  /* a forced configuration is invalid for this shape */
   GEMV_ERR_ALIGN = -7,   /* B or a not 2-byte aligned, or c not aligned to its element */
-  GEMV_ERR_NOMEM = -8    /* the split-K workspace could not be allocated */
+  GEMV_ERR_NOMEM = -8,   /* the split-K workspace could not be allocated */
+  GEMV_ERR_SCRATCH = -9  /* gemv_splitk_noalloc: grid_split * n exceeds GEMV_STATIC_SCRATCH_FLOATS */
 };
 
 /* Kernel variants (gemv_config.variant). */
@@ -223,6 +224,39 @@ int gemv_host(const void *B_host, const void *a_host, void *c_host, void *B_dev,
  * memory of at least 64 KiB).  Asynchronous on `stream`.
  */
 int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t stream);
+
+/* Capacity, in floats, of the static split-K scratch of gemv_splitk_noalloc(). */
+#define GEMV_STATIC_SCRATCH_FLOATS (1 << 20) /* 4 MiB per GPU */
+
+/*
+ * Split-K GEMV that allocates nothing.  The pages this library follows have
+ * no counterpart of this entry point; it exists for callers that must not
+ * allocate device memory while they run -- an inference engine's plugin code
+ * that is forbidden to call cudaMalloc during execution, a serving loop where
+ * a cudaMalloc would synchronize the device and stall its other streams, or
+ * a process whose device memory is handed out up front by its own allocator.
+ *
+ * Computes the same c = B @ a as gemv() (same arguments, same status codes,
+ * asynchronous on `stream`) with the tiles kernel split into `grid_split`
+ * k-segments (2 .. 64; a k too short for that many segments of 8 columns uses
+ * fewer, down to one), followed by the second pass that adds the fp32
+ * partials in segment order.  The partials live in a file-scope device array
+ * of GEMV_STATIC_SCRATCH_FLOATS floats that every GPU loading this library
+ * holds until the process exits; a call needing more than that
+ * (grid_split * n floats) returns GEMV_ERR_SCRATCH without launching.  No
+ * cudaMalloc, cudaFree or other allocating routine is called.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array:
+ * calls whose kernels overlap on the GPU (other streams, other threads,
+ * other host processes sharing the library's context) race on it and must
+ * be serialized by the caller.  The array keeps the last call's partial
+ * sums; nothing in it needs clearing, because each call writes every
+ * partial it reads.
+ */
+int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
+                        int grid_split, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

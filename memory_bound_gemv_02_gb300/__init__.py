@@ -11,7 +11,7 @@ built, every call raises.
 Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_prepare``,
 ``gemv_plan``, ``gemv_last_config``, ``gemv_status_string``,
 ``gemv_last_cuda_error``, ``gemv_debug_inject``, ``gemv_release``,
-``gemv_host``, ``gemv_probe_read``.
+``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``.
 """
 from __future__ import annotations
 
@@ -27,13 +27,15 @@ GEMV_F16, GEMV_BF16, GEMV_F16_OUT_F32, GEMV_BF16_OUT_F32 = 0, 1, 2, 3
 GEMV_OK = 0
 GEMV_ERR_ARG, GEMV_ERR_DTYPE, GEMV_ERR_ALIAS, GEMV_ERR_DEVICE = -1, -2, -3, -4
 GEMV_ERR_CUDA, GEMV_ERR_CONFIG, GEMV_ERR_ALIGN, GEMV_ERR_NOMEM = -5, -6, -7, -8
+GEMV_ERR_SCRATCH = -9
+GEMV_STATIC_SCRATCH_FLOATS = 1 << 20
 GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TILES = 0, 1, 2, 3
 GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B = 0, 1, 2
 
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
 ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_prepare", "gemv_plan", "gemv_last_config",
                 "gemv_status_string", "gemv_last_cuda_error", "gemv_debug_inject",
-                "gemv_release", "gemv_host", "gemv_probe_read")
+                "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc")
 
 
 class GemvConfig(ctypes.Structure):
@@ -90,6 +92,7 @@ def lib() -> ctypes.CDLL:
             L.gemv_release.argtypes = []
             L.gemv_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
             L.gemv_probe_read.argtypes = [vp, i64, vp, vp]
+            L.gemv_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
             for name in ENTRY_POINTS:
                 if name != "gemv_status_string":
                     getattr(L, name).restype = i32
@@ -244,3 +247,17 @@ def gemv_probe_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
     with torch.cuda.device(buf.device):
         st = lib().gemv_probe_read(buf.data_ptr(), nbytes, sink.data_ptr(), _stream_handle(stream))
     _check(st, "gemv_probe_read")
+
+
+def gemv_splitk_noalloc(B, a, c=None, out_fp32: bool = False, grid_split: int = 2, stream=None) -> torch.Tensor:
+    """Split-K GEMV whose partial sums live in the library's fixed device
+    scratch array instead of allocated memory (for callers that must not
+    allocate while they run).  Calls that overlap on the GPU share that
+    array and must not run concurrently."""
+    n, k, c = _operands(B, a, c, out_fp32)
+    with torch.cuda.device(B.device):
+        st = lib().gemv_splitk_noalloc(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
+                                       dtype_code(B.dtype, out_fp32), int(grid_split),
+                                       _stream_handle(stream))
+    _check(st, "gemv_splitk_noalloc")
+    return c

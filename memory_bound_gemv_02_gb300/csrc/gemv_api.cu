@@ -607,6 +607,7 @@ extern "C" const char *gemv_status_string(int status) {
     case GEMV_ERR_CONFIG: return "configuration invalid for this shape";
     case GEMV_ERR_ALIGN: return "pointer not aligned to its element type";
     case GEMV_ERR_NOMEM: return "split-K workspace allocation failed";
+    case GEMV_ERR_SCRATCH: return "split-K scratch needed (grid_split * n floats) exceeds the static scratch array";
     default: return "unknown status";
   }
 }
@@ -681,5 +682,118 @@ extern "C" int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaS
   pk<<<grid, 512, 0, stream>>>(static_cast<const uint4 *>(buf), bytes / 16, static_cast<uint32_t *>(sink));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
+  return GEMV_OK;
+}
+
+// --------------------------------------------------------------------------
+// Split-K without any allocation: the scratch lives in a fixed device array.
+//
+// Some callers must not allocate device memory while they run: an inference
+// engine's per-layer plugin code that is forbidden to call cudaMalloc during
+// execution, a serving loop where cudaMalloc would synchronize the device and
+// stall the other streams, or a process whose device memory is handed out up
+// front by its own allocator.  gemv_splitk_noalloc() serves them: the
+// split-K partial sums go to g_gemv_static_scratch, a file-scope device array
+// that exists on every GPU that loads this library, for the life of the
+// process.  The caller still passes B, a and c.
+static __device__ __align__(256) float g_gemv_static_scratch[GEMV_STATIC_SCRATCH_FLOATS];
+
+namespace gemvk {
+namespace {
+
+std::mutex g_static_mu;
+float *g_static_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch array on `dev`, which must be the
+// current device.  In host code the array's name is only a host-side stand-in,
+// so the address is looked up once per device with cudaGetSymbolAddress.
+int static_scratch_for(int dev, float **out) {
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (g_static_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_gemv_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    }
+    g_static_scratch_ptr[dev] = static_cast<float *>(p);
+  }
+  *out = g_static_scratch_ptr[dev];
+  return GEMV_OK;
+}
+
+}  // namespace
+}  // namespace gemvk
+
+extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
+                                   int grid_split, cudaStream_t stream) {
+  int st = validate(B, a, c, n, k, dtype);
+  if (st != GEMV_OK) return st;
+  if (grid_split < 2 || grid_split > kMaxGridSplit) return GEMV_ERR_CONFIG;
+  if (n == 0) return GEMV_OK;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  if (k == 0) {
+    e = cudaMemsetAsync(c, 0, (size_t)n * out_elem_bytes(dtype), stream);
+    return e == cudaSuccess ? GEMV_OK : cuda_fail(e);
+  }
+  const bool aligned = (((uintptr_t)B & 15u) == 0) && (k % 8 == 0);
+  gemv_config cfg{};
+  MainKernel mk = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const DeviceInfo &di = device_info_locked(dev);
+    if (!di.ok) return GEMV_ERR_DEVICE;
+    gemv_config forced{};
+    forced.variant = GEMV_VARIANT_TILES;
+    forced.grid_split = grid_split;
+    st = plan_impl(n, k, dtype, aligned, di.sm_count, &forced, &cfg);
+    if (st != GEMV_OK) return st;
+    if (cfg.smem_bytes > di.max_smem_optin) return GEMV_ERR_CONFIG;
+    mk = lookup_main(dtype, cfg, aligned);
+    if (mk == nullptr) return GEMV_ERR_CONFIG;
+    e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  // A short k can leave a single segment (no scratch needed at all).
+  if ((int64_t)cfg.grid_split * n > (int64_t)GEMV_STATIC_SCRATCH_FLOATS) return GEMV_ERR_SCRATCH;
+  float *ws = nullptr;
+  if (cfg.grid_split > 1) {
+    st = static_scratch_for(dev, &ws);
+    if (st != GEMV_OK) return st;
+  }
+  Params p;
+  p.B = static_cast<const uint16_t *>(B);
+  p.a = static_cast<const uint16_t *>(a);
+  p.c = c;
+  p.ws = ws;
+  p.n = n;
+  p.k = k;
+  p.kseg = cfg.k_segment;
+  p.base_off = (int32_t)(((uintptr_t)B >> 1) & 7u);
+  p.sg = cfg.grid_split;
+  p.sw = cfg.warp_split;
+  p.nrb = cfg.row_blocks;
+  p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
+  p.flags = 0;
+  // Every (segment, row) partial is written by the first kernel before the
+  // second reads it, so the scratch needs no clearing between calls.
+  mk<<<cfg.ctas, cfg.warps_per_cta * 32, cfg.smem_bytes, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cfg.grid_split > 1) {
+    ReduceKernel rk = lookup_reduce(dtype);
+    int64_t blocks = cdiv(n, kReduceThreads);
+    if (blocks > 65535) blocks = 65535;
+    rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  t_last = cfg;
+  t_has_last = true;
   return GEMV_OK;
 }

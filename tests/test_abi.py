@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol(gemv_lib):
 
 
 def test_status_strings(gemv_lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = gemv_lib.gemv_status_string(code)
         assert s and s != "unknown status"
     assert gemv_lib.gemv_status_string(-99) == "unknown status"
