@@ -115,6 +115,10 @@ enum {
  *  overlap        GEMV_OVERLAP_*.  Not part of the cached configuration: a
  *                 gemv_ex() call that sets only this field launches the
  *                 cached configuration of gemv() with the requested overlap.
+ *  l2_prefetch    tiles variant: before streaming a tile, each warp asks the
+ *                 L2 to prefetch its slice of the tile this many rounds
+ *                 ahead (one bulk prefetch per row slice; 0 = none, at most
+ *                 3; -1 forces 0 when forcing).
  */
 typedef struct gemv_config {
   int32_t variant;
@@ -129,7 +133,8 @@ typedef struct gemv_config {
   int32_t row_blocks;
   int32_t unroll;
   int32_t overlap;
-  int32_t reserved[3];
+  int32_t l2_prefetch;
+  int32_t reserved[2];
 } gemv_config;
 
 /*

@@ -46,7 +46,7 @@ class GemvConfig(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("k_segment", ctypes.c_int64), ("row_blocks", ctypes.c_int32),
                 ("unroll", ctypes.c_int32), ("overlap", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("l2_prefetch", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
     def to_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}

@@ -28,6 +28,7 @@ namespace {
 constexpr int64_t kMaxSegment = 32768;  // columns of a staged per CTA (64 KiB of shared memory)
 constexpr int kMaxGridSplit = 64;
 constexpr int kAutoVariant = GEMV_VARIANT_TILES;  // the planner's default family
+constexpr int kDefaultL2Prefetch = 0;              // tile rounds of L2 prefetch by default
 constexpr int kMaxSmemPerCta = 232448;  // 227 KiB, sm_100-family opt-in limit
 constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int64_t kSmemReservedPerCta = 1024;
@@ -233,6 +234,12 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     c.smem_bytes = (int32_t)(round_up(kseg + 24, 8) * 2 + 2LL * W * R * 4);
     c.launches = Sg > 1 ? 2 : 1;
     c.k_segment = kseg;
+    if (f->l2_prefetch) {
+      if (f->l2_prefetch < -1 || f->l2_prefetch > 3) return GEMV_ERR_CONFIG;
+      c.l2_prefetch = f->l2_prefetch < 0 ? 0 : f->l2_prefetch;
+    } else {
+      c.l2_prefetch = kDefaultL2Prefetch;
+    }
     best = c;
     have = true;
     if (f->warps_per_cta || c.ctas >= sm) break;
@@ -463,7 +470,8 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
     if (!di.ok) return GEMV_ERR_DEVICE;
     const bool is_forced = forced != nullptr && (forced->variant || forced->rows_per_warp ||
                                                  forced->warps_per_cta || forced->warp_split ||
-                                                 forced->grid_split || forced->ctas || forced->unroll);
+                                                 forced->grid_split || forced->ctas || forced->unroll ||
+                                                 forced->l2_prefetch);
     if (is_forced) {
       st = plan_impl(n, k, dtype, aligned, di.sm_count, forced, &cfg);
       if (st != GEMV_OK) return st;
@@ -502,7 +510,8 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
   p.sw = cfg.warp_split;
   p.nrb = cfg.row_blocks;
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
-  p.flags = (overlap == GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0;
+  p.flags = ((overlap == GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
+            (cfg.l2_prefetch << kFlagL2Shift);
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

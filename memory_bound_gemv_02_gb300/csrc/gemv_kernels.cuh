@@ -86,16 +86,49 @@ __device__ __forceinline__ void widen8(const uint4 &v, float (&f)[8]) {
   f[4] = p2.x; f[5] = p2.y; f[6] = p3.x; f[7] = p3.y;
 }
 
+// Packed fp32x2 FMA measured no faster than two fmaf on GB300 for this
+// kernel (the pair packing costs what the pairing saves); off by default.
+#ifndef GEMV_USE_FFMA2
+#define GEMV_USE_FFMA2 0
+#endif
+
+// Two independent fp32 fused multiply-adds in one instruction (sm_100+):
+// acc.x = fma(b.x, a.x, acc.x), acc.y = fma(b.y, a.y, acc.y), each rounded
+// once exactly as fmaf.
+__device__ __forceinline__ void ffma2(float &acc_x, float &acc_y, float b_x, float b_y, float a_x, float a_y) {
+#if GEMV_USE_FFMA2
+  unsigned long long acc, b, a;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(acc_x), "f"(acc_y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b_x), "f"(b_y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a_x), "f"(a_y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(b), "l"(a));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc_x), "=f"(acc_y) : "l"(acc));
+#else
+  acc_x = fmaf(b_x, a_x, acc_x);
+  acc_y = fmaf(b_y, a_y, acc_y);
+#endif
+}
+
 // Multiply-accumulate one 16-byte vector of B (8 elements) with the
-// matching widened a elements.  With NA accumulators, element e goes to
-// acc[(e / 2) % NA]; 4 accumulators give four independent chains of two.
+// matching widened a elements.  NA accumulator pairs (x for even, y for odd
+// elements): element pair q goes to pair (q % NA); 4 pairs give eight
+// independent chains of one.
 template <class T, int NA>
-__device__ __forceinline__ void fma8(const uint4 &b, const float (&af)[8], float (&acc)[NA]) {
+__device__ __forceinline__ void fma8(const uint4 &b, const float (&af)[8], float (&acc)[NA][2]) {
   const float2 p0 = T::pair(b.x), p1 = T::pair(b.y), p2 = T::pair(b.z), p3 = T::pair(b.w);
-  acc[0 % NA] = fmaf(p0.x, af[0], acc[0 % NA]); acc[0 % NA] = fmaf(p0.y, af[1], acc[0 % NA]);
-  acc[1 % NA] = fmaf(p1.x, af[2], acc[1 % NA]); acc[1 % NA] = fmaf(p1.y, af[3], acc[1 % NA]);
-  acc[2 % NA] = fmaf(p2.x, af[4], acc[2 % NA]); acc[2 % NA] = fmaf(p2.y, af[5], acc[2 % NA]);
-  acc[3 % NA] = fmaf(p3.x, af[6], acc[3 % NA]); acc[3 % NA] = fmaf(p3.y, af[7], acc[3 % NA]);
+  ffma2(acc[0 % NA][0], acc[0 % NA][1], p0.x, p0.y, af[0], af[1]);
+  ffma2(acc[1 % NA][0], acc[1 % NA][1], p1.x, p1.y, af[2], af[3]);
+  ffma2(acc[2 % NA][0], acc[2 % NA][1], p2.x, p2.y, af[4], af[5]);
+  ffma2(acc[3 % NA][0], acc[3 % NA][1], p3.x, p3.y, af[6], af[7]);
+}
+
+// Sum of the NA accumulator pairs (fixed order).
+template <int NA>
+__device__ __forceinline__ float acc_total(const float (&acc)[NA][2]) {
+  float v = acc[0][0] + acc[0][1];
+#pragma unroll
+  for (int q = 1; q < NA; ++q) v += acc[q][0] + acc[q][1];
+  return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -194,12 +227,12 @@ __device__ __forceinline__ void rows_aligned(const Params &p, const uint4 *as4, 
   for (int r = 0; r < R; ++r) roff[r] = (i0 + r < r1) ? r * kv : 0;
   // Independent fp32 accumulators: 4 for one row, 2 each for two rows, 1
   // each for four (the R rows already give independent chains).
-  constexpr int NA = (R == 1) ? 4 : (R == 2 ? 2 : 1);
-  float acc[R][NA];
+  constexpr int NA = (R == 1) ? 2 : 1;  // accumulator pairs per row
+  float acc[R][NA][2];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
 #pragma unroll
-    for (int q = 0; q < NA; ++q) acc[r][q] = 0.f;
+    for (int q = 0; q < NA; ++q) acc[r][q][0] = acc[r][q][1] = 0.f;
   }
   for (int t = t0 + lane; t < t1; t += 32 * U) {
     uint4 bv[U][R];
@@ -221,12 +254,7 @@ __device__ __forceinline__ void rows_aligned(const Params &p, const uint4 *as4, 
     }
   }
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    float v = acc[r][0];
-#pragma unroll
-    for (int q = 1; q < NA; ++q) v += acc[r][q];
-    out[r] = warp_sum(v);
-  }
+  for (int r = 0; r < R; ++r) out[r] = warp_sum(acc_total<NA>(acc[r]));
 }
 
 // General variant, one row.  The row's segment spans global 16-byte blocks
@@ -236,7 +264,7 @@ __device__ __forceinline__ void rows_aligned(const Params &p, const uint4 *as4, 
 // SH = 8 - off.  Blocks [t0, t1) are this warp's share.
 template <class T, int SH, int U>
 __device__ __forceinline__ void row_general(const uint4 *bal, const uint4 *as4, int64_t g0, int off, int64_t len,
-                                            int nt, int t0, int t1, int lane, float (&acc)[4]) {
+                                            int nt, int t0, int t1, int lane, float (&acc)[2][2]) {
   const int last_hi = (int)(len + off - 8 * (int64_t)(nt - 1));  // valid elements of the last block
   for (int t = t0 + lane; t < t1; t += 32 * U) {
     uint4 bv[U];
@@ -259,7 +287,7 @@ __device__ __forceinline__ void row_general(const uint4 *bal, const uint4 *as4, 
         }
         float af[8];
         widen8<T>(av, af);
-        fma8<T, 4>(b, af, acc);
+        fma8<T, 2>(b, af, acc);
       }
     }
   }
@@ -274,7 +302,7 @@ __device__ __forceinline__ float row_general_dispatch(const Params &p, const uin
   const int off = (int)(e0 & 7);
   const int nt = (int)((off + len + 7) >> 3);
   const int t0 = (int)((int64_t)nt * s / sw), t1 = (int)((int64_t)nt * (s + 1) / sw);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   switch (8 - off) {  // warp-uniform
     case 1: row_general<T, 1, U>(bal, as4, g0, off, len, nt, t0, t1, lane, acc); break;
     case 2: row_general<T, 2, U>(bal, as4, g0, off, len, nt, t0, t1, lane, acc); break;
@@ -285,7 +313,7 @@ __device__ __forceinline__ float row_general_dispatch(const Params &p, const uin
     case 7: row_general<T, 7, U>(bal, as4, g0, off, len, nt, t0, t1, lane, acc); break;
     default: row_general<T, 8, U>(bal, as4, g0, off, len, nt, t0, t1, lane, acc); break;
   }
-  return warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+  return warp_sum(acc_total<2>(acc));
 }
 
 // ----------------------------------------------------------- main kernel --

@@ -30,6 +30,12 @@ __device__ __forceinline__ void team_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Ask the L2 to fetch [p, p + bytes) (16-byte aligned, multiple of 16) from
+// HBM; no registers are held and nothing is returned.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Stage columns [j0, j0 + len) of a, shifted right by `off` elements:
 // as[x] = a[j0 + x - off] for off <= x < off + len, 0 for other x < as_elems.
 // Block t of a row that starts at offset `off` then multiplies as4[t].
@@ -71,11 +77,13 @@ __device__ __forceinline__ void tile_issue(const uint4 *bal, const int64_t (&g0)
 }
 
 // Multiply-accumulate one step's blocks with the staged (pre-shifted) a.
-// Unaligned rows: the first and last block of a row carry elements of the
-// neighbouring rows, which are zeroed first.
-template <class T, int U, int R, int NA, bool ALIGNED>
-__device__ __forceinline__ void tile_consume(const uint4 *as4, const uint4 (&bv)[U][R], int t, int t1, int nt,
-                                             int off, int last_hi, float (&acc)[R][NA]) {
+// No masking: for an unaligned row the first and last block also hold
+// elements of the neighbouring rows, but the staged a is zero at those
+// positions, so they add exactly 0 -- unless they are Inf or NaN (0 * Inf =
+// NaN).  That case can only turn the sum NaN and is redone by tile_redo().
+template <class T, int U, int R, int NA>
+__device__ __forceinline__ void tile_consume(const uint4 *as4, const uint4 (&bv)[U][R], int t, int t1,
+                                             float (&acc)[R][NA][2]) {
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int tt = t + 32 * u;
@@ -83,15 +91,26 @@ __device__ __forceinline__ void tile_consume(const uint4 *as4, const uint4 (&bv)
       float af[8];
       widen8<T>(as4[tt], af);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        uint4 b = bv[u][r];
-        if constexpr (!ALIGNED) {
-          if (tt == 0 || tt == nt - 1) b = keep_range(b, tt == 0 ? off : 0, tt == nt - 1 ? last_hi : 8);
-        }
-        fma8<T, NA>(b, af, acc[r]);
-      }
+      for (int r = 0; r < R; ++r) fma8<T, NA>(bv[u][r], af, acc[r]);
     }
   }
+}
+
+// The slow path of an unaligned row slice whose fast sum came out NaN:
+// stream the slice [t0, t1) of one row again with the neighbouring rows'
+// elements of the edge blocks (0 and nt - 1) zeroed.  Warp-uniform.
+template <class T>
+__device__ __forceinline__ float tile_redo(const uint4 *bal, const uint4 *as4, int64_t g0, int t0, int t1, int nt,
+                                        int off, int last_hi, int lane) {
+  float acc[1][2] = {{0.f, 0.f}};
+  for (int t = t0 + lane; t < t1; t += 32) {
+    uint4 b = ldg_stream(bal + g0 + t);
+    if (t == 0 || t == nt - 1) b = keep_range(b, t == 0 ? off : 0, t == nt - 1 ? last_hi : 8);
+    float af[8];
+    widen8<T>(as4[t], af);
+    fma8<T, 1>(b, af, acc);
+  }
+  return warp_sum(acc_total<1>(acc));
 }
 
 // Grid: blockIdx.x = c * sg + gs, c in [0, C) with C = p.nrb.  ALIGNED
@@ -102,7 +121,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   extern __shared__ __align__(16) uint4 smem4[];
   uint4 *as4 = smem4;
   float *ps = reinterpret_cast<float *>(smem4 + (p.as_elems >> 3));  // [2][W * R]
-  constexpr int NA = (R == 1) ? 4 : (R == 2 ? 2 : 1);
+  constexpr int NA = (R == 1) ? 2 : 1;  // accumulator pairs per row
 
   const int W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gs = blockIdx.x % p.sg;
@@ -135,6 +154,20 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     }
   };
 
+  // Bulk L2 prefetch of this warp's row slices of tile g (lane r < R
+  // issues row r's), `pf` rounds ahead of the tile being streamed.
+  const int pf = (p.flags >> kFlagL2Shift) & 3;
+  auto prefetch_tile = [&](int64_t g) {
+    if (g < ngroups && lane < R && t1 > t0) {
+      const int64_t j = g * RT + (int64_t)slot * R + lane;
+      if (j < nr) {
+        const int64_t i = NCLS * j + cls;
+        const int64_t gb = ((int64_t)p.base_off + i * p.k + j0) >> 3;
+        prefetch_l2(bal + gb + t0, (uint32_t)(t1 - t0) * 16u);
+      }
+    }
+  };
+
   // The first tile's first loads go out before a is staged, so the B
   // stream starts at once and the staging latency hides under it.  Under a
   // programmatic dependent launch with kFlagPrefetchB they even go out
@@ -152,6 +185,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     tile_issue<U, R>(bal, g0, valid, t0 + lane, t1, bv);
     prefetched = true;
   }
+  for (int m = 1; m <= pf; ++m) prefetch_tile(cq + (int64_t)m * Cq);
   if (early) wait_for_predecessor();
   stage_a_shifted(p, as4, j0, len, off);
   __syncthreads();
@@ -161,25 +195,28 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     int64_t g0[R];
     bool valid[R];
     rows_of(g, g0, valid);
-    float acc[R][NA];
+    if (pf > 0 && g > cq) prefetch_tile(g + (int64_t)pf * Cq);
+    float acc[R][NA][2];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
-      for (int q = 0; q < NA; ++q) acc[r][q] = 0.f;
+      for (int q = 0; q < NA; ++q) acc[r][q][0] = acc[r][q][1] = 0.f;
     }
     for (int t = t0 + lane; t < t1; t += 32 * U) {
       if (!prefetched) tile_issue<U, R>(bal, g0, valid, t, t1, bv);
       prefetched = false;
-      tile_consume<T, U, R, NA, ALIGNED>(as4, bv, t, t1, nt, off, last_hi, acc);
+      tile_consume<T, U, R, NA>(as4, bv, t, t1, acc);
     }
     prefetched = false;
     float v[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float x = acc[r][0];
+    for (int r = 0; r < R; ++r) v[r] = warp_sum(acc_total<NA>(acc[r]));
+    if constexpr (!ALIGNED) {
+      if (t0 == 0 || t1 == nt) {  // this slice holds a row edge
 #pragma unroll
-      for (int q = 1; q < NA; ++q) x += acc[r][q];
-      v[r] = warp_sum(x);
+        for (int r = 0; r < R; ++r)
+          if (valid[r] && isnan(v[r])) v[r] = tile_redo<T>(bal, as4, g0[r], t0, t1, nt, off, last_hi, lane);
+      }
     }
     const int64_t jb = g * RT + (int64_t)slot * R;
     if (S == 1) {

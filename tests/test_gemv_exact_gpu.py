@@ -27,7 +27,8 @@ CONFIGS = [None, {"variant": 2}, {"rows_per_warp": 4}, {"warps_per_cta": 4, "war
            {"grid_split": 3}, {"grid_split": 2, "warp_split": 8}, {"ctas": 3},
            {"variant": 3}, {"variant": 3, "warp_split": 4}, {"variant": 3, "rows_per_warp": 4, "unroll": 2},
            {"variant": 3, "rows_per_warp": 2, "unroll": 4, "warps_per_cta": 8},
-           {"variant": 3, "grid_split": 3, "warp_split": 2}, {"variant": 3, "ctas": 8}]
+           {"variant": 3, "grid_split": 3, "warp_split": 2}, {"variant": 3, "ctas": 8},
+           {"variant": 3, "l2_prefetch": 2}, {"variant": 3, "l2_prefetch": 1, "warp_split": 4, "overlap": 2}]
 
 
 def _run(B, a, out_fp32=False, config=None, c=None):

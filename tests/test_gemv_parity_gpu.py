@@ -109,6 +109,8 @@ FORCED = [
     {"ctas": 1}, {"ctas": 37, "rows_per_warp": 2},
     {"variant": 3}, {"variant": 3, "warp_split": 8}, {"variant": 3, "warp_split": 2, "warps_per_cta": 4},
     {"variant": 3, "rows_per_warp": 2, "unroll": 4}, {"variant": 3, "grid_split": 4},
+    {"variant": 3, "l2_prefetch": 1}, {"variant": 3, "l2_prefetch": 3, "warp_split": 2},
+    {"variant": 3, "l2_prefetch": 2, "rows_per_warp": 4, "unroll": 2, "overlap": 2},
 ]
 
 
@@ -121,7 +123,7 @@ def test_forced_configs_parity(cuda_dev, cfg, dtype):
         used = g.gemv_last_config()
         for key, v in cfg.items():
             if key not in ("ctas", "grid_split"):
-                assert used[key] == v
+                assert used[key] == v, key
         check_against_oracle(c, B, a, out_fp32, label=f"{cfg} {dtype} f32out={out_fp32}")
 
 
