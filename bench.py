@@ -337,6 +337,27 @@ def time_calls(L, calls, stream, steps, warmup):
     return e0.elapsed_time(e1) / 1e3, per
 
 
+def time_batch(calls, steps, warmup):
+    """Run `calls` round-robin back to back with CUDA events only at both
+    ends of the batch; return the elapsed seconds."""
+    import torch
+    for i in range(warmup):
+        fn, args = calls[i % len(calls)]
+        if fn(*args) != 0:
+            raise RuntimeError("gemv failed")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    torch.cuda._sleep(3_000_000)  # keep the GPU busy while the launches queue up
+    e0.record(s)
+    for i in range(steps):
+        fn, args = calls[i % len(calls)]
+        fn(*args)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
 def host_overhead_us(L, n, k, dt, dev, stream):
     """Host time of one cached-key gemv() call (enqueue only), in bursts of
     200 calls so the launch queue never fills; median over bursts."""
@@ -358,7 +379,9 @@ def host_overhead_us(L, n, k, dt, dev, stream):
 
 
 def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev):
-    """One shape: per-call device time (median over calls), GB/s, config."""
+    """One shape: µs per call three ways -- isolated (CUDA events around each
+    launch), back to back, and back to back with programmatic dependent
+    launch -- and the launch configuration."""
     import torch
 
     from memory_bound_gemv_02_gb300 import inputs
@@ -370,17 +393,27 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev):
     c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
     dt = g.dtype_code(B.dtype, out_fp32)
     s = torch.cuda.current_stream().cuda_stream
-    calls = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in Bs]
     g.gemv(B, a, c=c, out_fp32=out_fp32)
     cfg = g.gemv_last_config()
-    elapsed, per = time_calls(L, calls, s, steps, warmup)
-    med = statistics.median(per)
+    plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in Bs]
+    ov = g.GemvConfig()
+    ov.overlap = g.GEMV_OVERLAP_PDL_PREFETCH_B
+    pdl = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(ov), s)) for Bx in Bs]
+    _, per = time_calls(L, plain, s, steps, warmup)
+    el_plain = time_batch(plain, steps, warmup)
+    el_pdl = time_batch(pdl, steps, warmup)
+    iso = statistics.median(per) * 1e3
+    b2b = el_plain / steps * 1e6
+    b2b_pdl = el_pdl / steps * 1e6
     return {"n": n, "k": k, "dtype": dtype, "out": "f32" if out_fp32 else dtype, "dist": dist,
-            "us_per_call_median": round(med * 1e3, 3), "us_per_call_min": round(min(per) * 1e3, 3),
-            "us_per_call_p90": round(sorted(per)[int(0.9 * (len(per) - 1))] * 1e3, 3),
-            "stddev_over_median": round(statistics.pstdev(per) / med, 4),
-            "gbs": round(nbytes / (med / 1e3) / 1e9, 1), "bytes": nbytes, "b_copies": copies,
-            "config": cfg}
+            "bytes": nbytes, "b_copies": copies,
+            "us_isolated_median": round(iso, 3), "us_isolated_min": round(min(per) * 1e3, 3),
+            "stddev_over_median": round(statistics.pstdev(per) / statistics.median(per), 4),
+            "us_back_to_back": round(b2b, 3), "us_back_to_back_pdl": round(b2b_pdl, 3),
+            "gbs_isolated": round(nbytes / iso / 1e3, 1), "gbs_back_to_back": round(nbytes / b2b / 1e3, 1),
+            "gbs_back_to_back_pdl": round(nbytes / b2b_pdl / 1e3, 1),
+            "config": {kk: cfg[kk] for kk in ("variant", "rows_per_warp", "unroll", "warps_per_cta",
+                                              "warp_split", "grid_split", "ctas")}}
 
 
 def run_sweep(args, dev):
@@ -392,8 +425,8 @@ def run_sweep(args, dev):
     out = open(args.sweep, "w")
     for n, k, dtype, out_fp32, dist in SWEEP_SHAPES:
         r = bench_shape(g, L, n, k, dtype, out_fp32, dist, 0, args.sweep_steps, 20, dev)
-        r["pct_of_8tbps"] = round(100 * r["gbs"] / NOMINAL_HBM_GBS, 1)
-        r[f"pct_of_{kind}_peak"] = round(100 * r["gbs"] / peak, 1)
+        r["pct_of_8tbps_pdl"] = round(100 * r["gbs_back_to_back_pdl"] / NOMINAL_HBM_GBS, 1)
+        r[f"frac_of_{kind}_peak_pdl"] = round(r["gbs_back_to_back_pdl"] / peak, 4)
         out.write(json.dumps(r) + "\n")
         out.flush()
         print(json.dumps(r), file=sys.stderr, flush=True)
@@ -495,16 +528,8 @@ def run_ours(args, world, rank, local):
     # Context (untimed for `value`): the same calls without overlap, back to
     # back, and one at a time with CUDA events around each launch.
     plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in (B, B2)]
-    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(3_000_000)
-    e_a.record(stream)
     nplain = min(args.steps, 2000)
-    for i in range(nplain):
-        fn, cargs = plain[i % 2]
-        fn(*cargs)
-    e_b.record(stream)
-    torch.cuda.synchronize()
-    us_plain = e_a.elapsed_time(e_b) * 1e3 / nplain
+    us_plain = time_batch(plain, nplain, 10) / nplain * 1e6
     _, per_iso = time_calls(L, plain, s, 200, 10)
     us_iso = statistics.median(per_iso) * 1e3
 

@@ -3,11 +3,12 @@
 //
 // Differences from the row-per-warp kernel, both measured on GB300:
 //
-//  * Dense access order.  A CTA works on tiles of RT consecutive rows of its
-//    row class, and tile g of every CTA lies next to tile g of the others,
-//    so at any moment the whole GPU streams one narrow, contiguous window of
-//    B (the order a grid-stride copy uses), instead of thousands of
-//    unrelated row streams spread over the matrix.
+//  * Dense access order.  The rows of a row class are dealt to its CTAs
+//    round-robin and each CTA streams its rows in tiles of RT, so local tile
+//    g of every CTA covers one contiguous block of rows: at any moment the
+//    whole GPU streams one narrow window of B (the order a grid-stride copy
+//    uses), instead of thousands of unrelated row streams spread over the
+//    matrix, and CTA loads differ by at most one row.
 //  * One code path for any alignment.  The rows of B start at element
 //    offset (base + i*k) mod 8 inside a 16-byte block, which depends only on
 //    i mod 8.  CTAs are assigned one residue class of rows each, so every
@@ -36,30 +37,56 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Source vector q of the segment: a[j0 + 8q .. j0 + 8q + 7], zero outside
+// the segment's columns [0, len).  `aj` = a + j0; `vec_ok`: aj is 16-byte
+// aligned, so whole vectors can be loaded at once.
+__device__ __forceinline__ uint4 a_vec(const uint16_t *aj, int64_t q, int64_t len, bool vec_ok) {
+  const int64_t jb = 8 * q;
+  if (q < 0 || jb >= len) return zero4();
+  if (vec_ok && jb + 8 <= len) return __ldg(reinterpret_cast<const uint4 *>(aj + jb));
+  uint32_t w[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int64_t j_lo = jb + 2 * h, j_hi = jb + 2 * h + 1;
+    const uint32_t lo = (j_lo < len) ? (uint32_t)__ldg(aj + j_lo) : 0u;
+    const uint32_t hi = (j_hi < len) ? (uint32_t)__ldg(aj + j_hi) : 0u;
+    w[h] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// as4[q] = elements [SH, SH + 8) of source vectors (q - 1) ++ q, i.e. the
+// segment shifted right by off = 8 - SH elements.
+template <int SH>
+__device__ __forceinline__ void stage_shift_loop(uint4 *as4, int nvec, const uint16_t *aj, int64_t len, bool vec_ok) {
+  for (int q = threadIdx.x; q < nvec; q += blockDim.x) {
+    const uint4 hi = a_vec(aj, q, len, vec_ok);
+    if constexpr (SH == 8) {
+      as4[q] = hi;
+    } else {
+      as4[q] = window<SH>(a_vec(aj, q - 1, len, vec_ok), hi);
+    }
+  }
+}
+
 // Stage columns [j0, j0 + len) of a, shifted right by `off` elements:
 // as[x] = a[j0 + x - off] for off <= x < off + len, 0 for other x < as_elems.
 // Block t of a row that starts at offset `off` then multiplies as4[t].
+// Built from whole 16-byte loads of a plus a register shift (one code path
+// per offset, chosen once per CTA).
 __device__ __forceinline__ void stage_a_shifted(const Params &p, uint4 *as4, int64_t j0, int64_t len, int off) {
   const int nvec = p.as_elems >> 3;
   const uint16_t *aj = p.a + j0;
-  const bool vec_ok = off == 0 && (reinterpret_cast<uintptr_t>(aj) & 15u) == 0;
-  for (int q = threadIdx.x; q < nvec; q += blockDim.x) {
-    const int64_t jb = 8 * (int64_t)q - off;  // segment column of element 0 of this vector
-    uint4 v;
-    if (vec_ok && jb + 8 <= len) {
-      v = __ldg(reinterpret_cast<const uint4 *>(aj + jb));
-    } else {
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int64_t j_lo = jb + 2 * h, j_hi = jb + 2 * h + 1;
-        const uint32_t lo = (j_lo >= 0 && j_lo < len) ? (uint32_t)__ldg(aj + j_lo) : 0u;
-        const uint32_t hi = (j_hi >= 0 && j_hi < len) ? (uint32_t)__ldg(aj + j_hi) : 0u;
-        w[h] = lo | (hi << 16);
-      }
-      v = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    as4[q] = v;
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(aj) & 15u) == 0;
+  switch (8 - off) {
+    case 1: stage_shift_loop<1>(as4, nvec, aj, len, vec_ok); break;
+    case 2: stage_shift_loop<2>(as4, nvec, aj, len, vec_ok); break;
+    case 3: stage_shift_loop<3>(as4, nvec, aj, len, vec_ok); break;
+    case 4: stage_shift_loop<4>(as4, nvec, aj, len, vec_ok); break;
+    case 5: stage_shift_loop<5>(as4, nvec, aj, len, vec_ok); break;
+    case 6: stage_shift_loop<6>(as4, nvec, aj, len, vec_ok); break;
+    case 7: stage_shift_loop<7>(as4, nvec, aj, len, vec_ok); break;
+    default: stage_shift_loop<8>(as4, nvec, aj, len, vec_ok); break;
   }
 }
 
@@ -138,19 +165,25 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
 
   const uint4 *bal = reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p.B) & ~(uintptr_t)15);
   const int S = p.sw, slots = W / S, slot = warp / S, s = warp % S;
-  const int RT = slots * R;  // rows of the class per tile
+  const int RT = slots * R;  // rows per tile
   const int L = (nt + S - 1) / S;
   const int t0 = s * L < nt ? s * L : nt;
   const int t1 = t0 + L < nt ? t0 + L : nt;
-  const int64_t ngroups = (nr + RT - 1) / RT;
+  // Rows of the class are dealt to the class's Cq CTAs round-robin: this CTA
+  // owns class rows j = cq + Cq*m, m < nloc (so CTA loads differ by at most
+  // one row), streamed as local tiles of RT consecutive m.  Local tile g of
+  // every CTA covers class rows [Cq*RT*g, Cq*RT*(g+1)): one contiguous window
+  // of B at a time across the GPU.
+  const int64_t nloc = nr > cq ? (nr - cq + Cq - 1) / Cq : 0;
+  const int64_t ngroups = (nloc + RT - 1) / RT;
+  auto row_of = [&](int64_t m) -> int64_t { return NCLS * (cq + (int64_t)Cq * m) + cls; };
 
   auto rows_of = [&](int64_t g, int64_t (&g0)[R], bool (&valid)[R]) {
-    const int64_t jb = g * RT + (int64_t)slot * R;
+    const int64_t mb = g * RT + (int64_t)slot * R;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      valid[r] = (jb + r) < nr;
-      const int64_t i = NCLS * (jb + r) + cls;
-      g0[r] = valid[r] ? (((int64_t)p.base_off + i * p.k + j0) >> 3) : 0;
+      valid[r] = (mb + r) < nloc;
+      g0[r] = valid[r] ? (((int64_t)p.base_off + row_of(mb + r) * p.k + j0) >> 3) : 0;
     }
   };
 
@@ -159,10 +192,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   const int pf = (p.flags >> kFlagL2Shift) & 3;
   auto prefetch_tile = [&](int64_t g) {
     if (g < ngroups && lane < R && t1 > t0) {
-      const int64_t j = g * RT + (int64_t)slot * R + lane;
-      if (j < nr) {
-        const int64_t i = NCLS * j + cls;
-        const int64_t gb = ((int64_t)p.base_off + i * p.k + j0) >> 3;
+      const int64_t m = g * RT + (int64_t)slot * R + lane;
+      if (m < nloc) {
+        const int64_t gb = ((int64_t)p.base_off + row_of(m) * p.k + j0) >> 3;
         prefetch_l2(bal + gb + t0, (uint32_t)(t1 - t0) * 16u);
       }
     }
@@ -178,24 +210,24 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   if (!early) wait_for_predecessor();
   uint4 bv[U][R];
   bool prefetched = false;
-  if (cq < ngroups) {
+  if (ngroups > 0) {
     int64_t g0[R];
     bool valid[R];
-    rows_of(cq, g0, valid);
+    rows_of(0, g0, valid);
     tile_issue<U, R>(bal, g0, valid, t0 + lane, t1, bv);
     prefetched = true;
   }
-  for (int m = 1; m <= pf; ++m) prefetch_tile(cq + (int64_t)m * Cq);
+  for (int m = 1; m <= pf; ++m) prefetch_tile(m);
   if (early) wait_for_predecessor();
   stage_a_shifted(p, as4, j0, len, off);
   __syncthreads();
 
   int buf = 0;
-  for (int64_t g = cq; g < ngroups; g += Cq) {
+  for (int64_t g = 0; g < ngroups; ++g) {
     int64_t g0[R];
     bool valid[R];
     rows_of(g, g0, valid);
-    if (pf > 0 && g > cq) prefetch_tile(g + (int64_t)pf * Cq);
+    if (pf > 0 && g > 0) prefetch_tile(g + pf);
     float acc[R][NA][2];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -218,12 +250,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
           if (valid[r] && isnan(v[r])) v[r] = tile_redo<T>(bal, as4, g0[r], t0, t1, nt, off, last_hi, lane);
       }
     }
-    const int64_t jb = g * RT + (int64_t)slot * R;
+    const int64_t mb = g * RT + (int64_t)slot * R;
     if (S == 1) {
       if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
-          if (valid[r]) store_out<T, OUT_F32>(p, gs, NCLS * (jb + r) + cls, v[r]);
+          if (valid[r]) store_out<T, OUT_F32>(p, gs, row_of(mb + r), v[r]);
       }
     } else {
       float *pb = ps + buf * (W * R);
@@ -233,11 +265,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
       }
       team_barrier(1 + slot, S * 32);
       if (s == 0 && lane < R) {
-        const int64_t j = jb + lane;
-        if (j < nr) {
+        const int64_t m = mb + lane;
+        if (m < nloc) {
           float sum = 0.f;
           for (int s2 = 0; s2 < S; ++s2) sum += pb[(slot * R + lane) * S + s2];
-          store_out<T, OUT_F32>(p, gs, NCLS * j + cls, sum);
+          store_out<T, OUT_F32>(p, gs, row_of(m), sum);
         }
       }
       buf ^= 1;

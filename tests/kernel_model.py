@@ -137,22 +137,25 @@ def replay_tiles(n, k, cfg, base_off=0):
         assert nt <= as_elems // 8
         RT = slots * R
         L = -(-nt // S)
-        ngroups = -(-nr // RT)
+        nloc = -(-(nr - cq) // Cq) if nr > cq else 0
+        ngroups = -(-nloc // RT)
         stage_x = np.arange(8 * nt)
         stage_col = stage_x - off  # segment column held by staged element x
-        for g in range(cq, ngroups, Cq):
+        for g in range(ngroups):
             for warp in range(W):
                 slot, s = divmod(warp, S)
-                jb = g * RT + slot * R
+                mb = g * RT + slot * R
                 t0 = min(s * L, nt)
                 t1 = min(t0 + L, nt)
                 if S > 1:
                     for r in range(R):
                         assert 0 <= (slot * R + r) * S + s < W * R
                 for r in range(R):
-                    j = jb + r
-                    if j >= nr:
+                    m = mb + r
+                    if m >= nloc:
                         continue
+                    j = cq + Cq * m
+                    assert j < nr
                     i = NCLS * j + cls
                     assert i < n
                     e0 = base_off + i * k + j0
@@ -174,9 +177,9 @@ def replay_tiles(n, k, cfg, base_off=0):
                     col_stage = stage_col[8 * tt + p]
                     assert (col_B[valid] == col_stage[valid]).all()
                     assert (col_B[valid] >= 0).all() and (col_B[valid] < seglen).all()
-                    # masked-off staged entries must be zero-filled (outside the segment)
-                    if aligned:
-                        assert ((col_stage >= 0) & (col_stage < seglen)).all()
+                    # outside the row the staged a must be zero (the kernel relies on it)
+                    outside = ~valid
+                    assert ((col_stage[outside] < 0) | (col_stage[outside] >= seglen)).all()
                     np.add.at(cover[i], j0 + col_B[valid], 1)
                     if Sg > 1:
                         ws_rows.add(gs * n + i)
@@ -184,3 +187,22 @@ def replay_tiles(n, k, cfg, base_off=0):
     if Sg > 1:
         assert len(ws_rows) == Sg * n
     return {"ctas": ctas}
+
+
+def staged_shifted(a, j0, seglen, off, as_elems):
+    """Host model of the tiles kernel's staging: output vector q is elements
+    [8 - off, 16 - off) of source vectors (q - 1) ++ q, source vector q being
+    a[j0 + 8q .. j0 + 8q + 7] with zeros outside the segment."""
+    def src(q):
+        v = np.zeros(8, dtype=a.dtype)
+        for e in range(8):
+            j = 8 * q + e
+            if q >= 0 and 0 <= j < seglen:
+                v[e] = a[j0 + j]
+        return v
+    out = np.zeros(as_elems, dtype=a.dtype)
+    sh = 8 - off
+    for q in range(as_elems // 8):
+        pair = np.concatenate([src(q - 1), src(q)])
+        out[8 * q: 8 * q + 8] = pair[sh: sh + 8]
+    return out

@@ -166,3 +166,19 @@ def test_tiles_plan_invariants(gemv_lib, n, k, aligned):
 def test_tiles_planner_choice_replay_medium(gemv_lib, n, k, aligned):
     cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 3})
     kernel_model.replay(n, k, cfg, base_off=0 if aligned else 5)
+
+
+@pytest.mark.parametrize("off", range(8))
+@pytest.mark.parametrize("j0,seglen,k", [(0, 37, 37), (8, 20, 40), (16, 7169 - 16, 7169), (0, 8, 8)])
+def test_shifted_staging_model(off, j0, seglen, k):
+    """The vector-plus-shift staging equals the definition
+    as[x] = a[j0 + x - off] for off <= x < off + seglen, 0 elsewhere."""
+    import numpy as np
+    a = np.arange(1, k + 1, dtype=np.int64)
+    as_elems = -(-(seglen + 24) // 8) * 8
+    got = kernel_model.staged_shifted(a, j0, seglen, off, as_elems)
+    want = np.zeros(as_elems, dtype=np.int64)
+    for x in range(as_elems):
+        if off <= x < off + seglen:
+            want[x] = a[j0 + x - off]
+    assert (got == want).all()
