@@ -79,11 +79,16 @@ enum {
                                  while the preceding kernel drains; it waits for that
                                  kernel's completion (and its memory) before reading or
                                  writing any global memory */
-  GEMV_OVERLAP_PDL_PREFETCH_B = 2 /* as GEMV_OVERLAP_PDL, and each CTA streams its first tile
+  GEMV_OVERLAP_PDL_PREFETCH_B = 2, /* as GEMV_OVERLAP_PDL, and each CTA streams its first tile
                                  of B into registers before waiting.  The caller guarantees
                                  that no work still running on the stream writes B (true
                                  for weights); a and c are still accessed only after the
                                  wait */
+  GEMV_OVERLAP_PDL_PREFETCH_BA = 3 /* as GEMV_OVERLAP_PDL_PREFETCH_B, and a is also read
+                                 (staged) before waiting: the caller guarantees that no work
+                                 still running on the stream writes B or a -- e.g. several
+                                 GEMVs on one input vector (Q/K/V or gate/up projections).
+                                 Only the writes of c wait for the predecessor */
 };
 
 /*

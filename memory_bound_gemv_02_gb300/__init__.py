@@ -30,7 +30,7 @@ GEMV_ERR_CUDA, GEMV_ERR_CONFIG, GEMV_ERR_ALIGN, GEMV_ERR_NOMEM = -5, -6, -7, -8
 GEMV_ERR_SCRATCH = -9
 GEMV_STATIC_SCRATCH_FLOATS = 1 << 20
 GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TILES = 0, 1, 2, 3
-GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B = 0, 1, 2
+GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B, GEMV_OVERLAP_PDL_PREFETCH_BA = 0, 1, 2, 3
 
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
 ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_prepare", "gemv_plan", "gemv_last_config",

@@ -459,7 +459,7 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
   }
   const bool aligned = (((uintptr_t)B & 15u) == 0) && (k % 8 == 0);
   const int overlap = forced ? forced->overlap : GEMV_OVERLAP_NONE;
-  if (overlap < GEMV_OVERLAP_NONE || overlap > GEMV_OVERLAP_PDL_PREFETCH_B) return GEMV_ERR_CONFIG;
+  if (overlap < GEMV_OVERLAP_NONE || overlap > GEMV_OVERLAP_PDL_PREFETCH_BA) return GEMV_ERR_CONFIG;
 
   gemv_config cfg{};
   float *ws = nullptr;
@@ -510,7 +510,8 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
   p.sw = cfg.warp_split;
   p.nrb = cfg.row_blocks;
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
-  p.flags = ((overlap == GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
+  p.flags = ((overlap >= GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
+            ((overlap == GEMV_OVERLAP_PDL_PREFETCH_BA) ? kFlagPrefetchA : 0) |
             (cfg.l2_prefetch << kFlagL2Shift);
 
   cudaLaunchAttribute attr[1];

@@ -20,7 +20,7 @@ struct Params {
   int32_t sw;         // warp split (warps per row inside a CTA)
   int32_t nrb;        // row blocks = gridDim.x / sg
   int32_t as_elems;   // staged a elements per CTA (multiple of 8, >= kseg + 24)
-  int32_t flags;      // kFlagPrefetchB | (L2 prefetch rounds << kFlagL2Shift)
+  int32_t flags;      // kFlagPrefetchB | kFlagPrefetchA | (L2 prefetch rounds << kFlagL2Shift)
   // Tiles kernel: sw = S (warps per row, slices), nrb = C (CTAs per k-segment).
 };
 
@@ -47,5 +47,6 @@ inline int unroll_for_rows(int R) { return R == 1 ? 8 : (R == 2 ? 4 : 2); }
 constexpr int kMaxThreads = 512;  // launch bound of the main kernel
 constexpr int kFlagPrefetchB = 1;
 constexpr int kFlagL2Shift = 1;  // 2 bits: tile rounds of bulk L2 prefetch ahead
+constexpr int kFlagPrefetchA = 8;  // stage a before waiting on the predecessor
 
 }  // namespace gemvk

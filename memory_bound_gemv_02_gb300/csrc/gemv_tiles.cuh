@@ -218,9 +218,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     prefetched = true;
   }
   for (int m = 1; m <= pf; ++m) prefetch_tile(m);
-  if (early) wait_for_predecessor();
+  // a is staged before the wait only when the caller promised that the
+  // predecessor does not write it (kFlagPrefetchA); c is always written
+  // after the wait.
+  const bool early_a = early && (p.flags & kFlagPrefetchA) != 0;
+  if (early && !early_a) wait_for_predecessor();
   stage_a_shifted(p, as4, j0, len, off);
   __syncthreads();
+  if (early_a) wait_for_predecessor();
 
   int buf = 0;
   for (int64_t g = 0; g < ngroups; ++g) {

@@ -325,5 +325,27 @@ def test_overlap_uses_cached_plan(cuda_dev):
     assert got["overlap"] == 2
     assert {k: v for k, v in got.items() if k != "overlap"} == {k: v for k, v in base.items() if k != "overlap"}
     with pytest.raises(g.GemvError) as ei:
-        g.gemv_ex(B, a, config={"overlap": 3})
+        g.gemv_ex(B, a, config={"overlap": 4})
     assert ei.value.status == g.GEMV_ERR_CONFIG
+
+
+@pytest.mark.parametrize("variant", [None, 3, 1])
+def test_overlap_prefetch_ba_shared_input(cuda_dev, variant):
+    """GEMV_OVERLAP_PDL_PREFETCH_BA (B and a promised unwritten by the work in
+    flight): several GEMVs on one input vector, e.g. the projections of one
+    activation, including consecutive calls that write the same c."""
+    cfg = {"overlap": 3}
+    if variant:
+        cfg["variant"] = variant
+    n, k = 3000, 4104
+    _, a = inputs.make_inputs(1, k, "bf16", "uniform", 8, cuda_dev)
+    Bs = [inputs.make_inputs(n, k, "bf16", "uniform", 20 + i, cuda_dev)[0] for i in range(4)]
+    outs = [g.gemv_ex(B, a, config=cfg) for B in Bs]
+    c = torch.empty(n, dtype=torch.bfloat16, device=cuda_dev)
+    for _ in range(3):
+        for B in Bs:
+            g.gemv_ex(B, a, c=c, config=cfg)
+    torch.cuda.synchronize()
+    for i, B in enumerate(Bs):
+        check_against_oracle(outs[i], B, a, False, label=f"shared input, B{i}")
+    check_against_oracle(c, Bs[-1], a, False, label="last writer of c")
