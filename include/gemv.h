@@ -176,6 +176,51 @@ int gemv(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
 int gemv_ex(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
             const gemv_config *forced, cudaStream_t stream);
 
+/* Activations of the fused epilogue. */
+enum {
+  GEMV_ACT_NONE = 0,
+  GEMV_ACT_RELU = 1,    /* max(y, 0) */
+  GEMV_ACT_SIGMOID = 2, /* 1 / (1 + exp(-y)) */
+  GEMV_ACT_SILU = 3     /* y / (1 + exp(-y)) */
+};
+
+/* Element type of the epilogue's bias vector. */
+enum { GEMV_BIAS_INPUT_TYPE = 0, GEMV_BIAS_F32 = 1 };
+
+/*
+ * Epilogue fused into the GEMV's single store (the register epilogue of the
+ * TileLang optimization guide, "Epilogue Fusion"):
+ *
+ *     c[i] = act(alpha * (B @ a)[i] + beta * bias[i])
+ *
+ * computed in fp32 on the fp32 row total and rounded once to the output
+ * type.  bias (n elements, device memory, not overlapping c) may be NULL.
+ * alpha = 1, bias = NULL, activation = GEMV_ACT_NONE is plain gemv().
+ */
+typedef struct gemv_epilogue {
+  float alpha;
+  float beta;
+  const void *bias;
+  int32_t bias_dtype;  /* GEMV_BIAS_INPUT_TYPE (fp16/bf16 as B) or GEMV_BIAS_F32 */
+  int32_t activation;  /* GEMV_ACT_* */
+} gemv_epilogue;
+
+/*
+ * GEMV over a row-strided B with a fused epilogue:
+ *
+ *     c[i] = act(alpha * sum_{j<k} B[i*ldb + j] * a[j] + beta * bias[i])
+ *
+ * ldb >= k is B's row stride in elements (row i starts at B + i*ldb); the
+ * elements between k and ldb are never used (they may hold anything,
+ * including NaN).  epilogue may be NULL (identity); config as in gemv_ex()
+ * (may be NULL; may set `overlap`).  Same status codes as gemv(), plus
+ * GEMV_ERR_ARG for ldb < k or an unknown activation/bias type,
+ * GEMV_ERR_ALIGN for a misaligned bias and GEMV_ERR_ALIAS for a bias
+ * overlapping c.  k == 0 gives act(beta * bias[i]) (the empty sum is 0).
+ */
+int gemv_fused(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_t k, int dtype,
+               const gemv_epilogue *epilogue, const gemv_config *config, cudaStream_t stream);
+
 /*
  * Build and cache the configuration gemv() would use for (n, k, dtype) on
  * the current device, for B with the given alignment (b_aligned16 != 0:

@@ -8,7 +8,7 @@ module only marshals torch tensors into pointers, sizes and the current
 stream.  There is no CPU or PyTorch fallback: if the library has not been
 built, every call raises.
 
-Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_prepare``,
+Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_fused``, ``gemv_prepare``,
 ``gemv_plan``, ``gemv_last_config``, ``gemv_status_string``,
 ``gemv_last_cuda_error``, ``gemv_debug_inject``, ``gemv_release``,
 ``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``.
@@ -31,9 +31,12 @@ GEMV_ERR_SCRATCH = -9
 GEMV_STATIC_SCRATCH_FLOATS = 1 << 20
 GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TILES = 0, 1, 2, 3
 GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B, GEMV_OVERLAP_PDL_PREFETCH_BA = 0, 1, 2, 3
+GEMV_ACT_NONE, GEMV_ACT_RELU, GEMV_ACT_SIGMOID, GEMV_ACT_SILU = 0, 1, 2, 3
+GEMV_BIAS_INPUT_TYPE, GEMV_BIAS_F32 = 0, 1
+ACTIVATIONS = {"none": GEMV_ACT_NONE, "relu": GEMV_ACT_RELU, "sigmoid": GEMV_ACT_SIGMOID, "silu": GEMV_ACT_SILU}
 
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
-ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_prepare", "gemv_plan", "gemv_last_config",
+ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_fused", "gemv_prepare", "gemv_plan", "gemv_last_config",
                 "gemv_status_string", "gemv_last_cuda_error", "gemv_debug_inject",
                 "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc")
 
@@ -50,6 +53,12 @@ class GemvConfig(ctypes.Structure):
 
     def to_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+class GemvEpilogue(ctypes.Structure):
+    """Mirror of ``gemv_epilogue`` in include/gemv.h."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("bias_dtype", ctypes.c_int32), ("activation", ctypes.c_int32)]
 
 
 class GemvError(RuntimeError):
@@ -82,6 +91,7 @@ def lib() -> ctypes.CDLL:
             cfgp = ctypes.POINTER(GemvConfig)
             L.gemv.argtypes = [vp, vp, vp, i64, i64, i32, vp]
             L.gemv_ex.argtypes = [vp, vp, vp, i64, i64, i32, cfgp, vp]
+            L.gemv_fused.argtypes = [vp, i64, vp, vp, i64, i64, i32, ctypes.POINTER(GemvEpilogue), cfgp, vp]
             L.gemv_prepare.argtypes = [i64, i64, i32, i32, vp]
             L.gemv_plan.argtypes = [i64, i64, i32, i32, i32, cfgp, cfgp]
             L.gemv_last_config.argtypes = [cfgp]
@@ -178,6 +188,49 @@ def gemv_ex(B, a, c=None, out_fp32: bool = False, config=None, stream=None) -> t
         st = lib().gemv_ex(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
                            dtype_code(B.dtype, out_fp32), _config_arg(config), _stream_handle(stream))
     _check(st, "gemv_ex")
+    return c
+
+
+def gemv_fused(B, a, c=None, out_fp32: bool = False, alpha: float = 1.0, beta: float = 1.0, bias=None,
+               activation: str = "none", config=None, stream=None) -> torch.Tensor:
+    """c = act(alpha * (B @ a) + beta * bias), fused into the GEMV's store.
+    ``B`` may be a row-strided view (stride (ldb, 1) with ldb >= k: rows of a
+    larger matrix); ``bias`` (optional) is a CUDA tensor of n elements in B's
+    dtype or float32; ``activation`` is 'none', 'relu', 'sigmoid' or 'silu'."""
+    if B.dim() != 2 or a.dim() != 1 or B.shape[1] != a.shape[0]:
+        raise ValueError(f"shape mismatch: B {tuple(B.shape)}, a {tuple(a.shape)}")
+    n, k = B.shape
+    if n > 0 and k > 0 and (B.stride(1) != 1 or B.stride(0) < k):
+        raise ValueError("B must have unit column stride and row stride >= k")
+    ldb = B.stride(0) if n > 1 else k
+    out_dtype = torch.float32 if out_fp32 else B.dtype
+    if c is None:
+        c = torch.empty(n, dtype=out_dtype, device=B.device)
+    if not (B.is_cuda and a.is_cuda and c.is_cuda) or c.dtype != out_dtype or c.shape != (n,):
+        raise ValueError("B, a, c must be CUDA tensors; c of shape (n,) and the output dtype")
+    if B.dtype != a.dtype or (k > 1 and a.stride(0) != 1) or (n > 1 and c.stride(0) != 1):
+        raise ValueError("a must be contiguous with B's dtype; c contiguous")
+    if B.device != a.device or B.device != c.device:
+        raise ValueError("B, a and c must be on the same device")
+    ep = GemvEpilogue()
+    ep.alpha = float(alpha)
+    ep.beta = float(beta)
+    ep.activation = ACTIVATIONS[activation]
+    if bias is not None:
+        if not bias.is_cuda or bias.shape != (n,) or (n > 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous CUDA tensor of shape (n,)")
+        if bias.dtype == torch.float32:
+            ep.bias_dtype = GEMV_BIAS_F32
+        elif bias.dtype == B.dtype:
+            ep.bias_dtype = GEMV_BIAS_INPUT_TYPE
+        else:
+            raise TypeError("bias must be float32 or B's dtype")
+        ep.bias = bias.data_ptr()
+    with torch.cuda.device(B.device):
+        st = lib().gemv_fused(B.data_ptr(), ldb, a.data_ptr(), c.data_ptr(), n, k,
+                              dtype_code(B.dtype, out_fp32), ctypes.byref(ep), _config_arg(config),
+                              _stream_handle(stream))
+    _check(st, "gemv_fused")
     return c
 
 

@@ -415,30 +415,50 @@ bool overlaps(const void *p, int64_t pbytes, const void *q, int64_t qbytes) {
   return a0 < b1 && b0 < a1;
 }
 
-// Checks that need no CUDA call.  Returns GEMV_OK or an error; sets *done
-// when nothing has to be launched (n == 0).
-int validate(const void *B, const void *a, const void *c, int64_t n, int64_t k, int dtype) {
+// Checks that need no CUDA call (row stride ldb >= k).  Returns GEMV_OK or
+// an error; n == 0 passes (nothing will be launched).
+int validate_ld(const void *B, int64_t ldb, const void *a, const void *c, int64_t n, int64_t k, int dtype) {
   if (dtype < 0 || dtype > 3) return GEMV_ERR_DTYPE;
   if (n < 0 || k < 0 || k > INT32_MAX) return GEMV_ERR_ARG;
+  if (ldb < k || ldb > INT32_MAX) return GEMV_ERR_ARG;
   if (n == 0) return GEMV_OK;
   if (c == nullptr) return GEMV_ERR_ARG;
   if (k > 0 && (B == nullptr || a == nullptr)) return GEMV_ERR_ARG;
   const int oe = out_elem_bytes(dtype);
   if (((uintptr_t)c % (uintptr_t)oe) != 0) return GEMV_ERR_ALIGN;
   if (k > 0 && (((uintptr_t)B & 1u) || ((uintptr_t)a & 1u))) return GEMV_ERR_ALIGN;
-  if (n > INT64_MAX / (k > 0 ? k : 1) / 2) return GEMV_ERR_ARG;
+  if (n > INT64_MAX / (ldb > 0 ? ldb : 1) / 2) return GEMV_ERR_ARG;
   if (k > 0) {
     const int64_t cb = n * oe;
-    if (overlaps(c, cb, B, n * k * 2) || overlaps(c, cb, a, k * 2)) return GEMV_ERR_ALIAS;
+    const int64_t bb = ((n - 1) * ldb + k) * 2;
+    if (overlaps(c, cb, B, bb) || overlaps(c, cb, a, k * 2)) return GEMV_ERR_ALIAS;
   }
   return GEMV_OK;
 }
 
-int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, const gemv_config *forced,
-        cudaStream_t stream) {
+int validate(const void *B, const void *a, const void *c, int64_t n, int64_t k, int dtype) {
+  return validate_ld(B, k, a, c, n, k, dtype);
+}
+
+Epilogue identity_epilogue() {
+  Epilogue ep;
+  ep.alpha = 1.f;
+  ep.beta = 0.f;
+  ep.bias = nullptr;
+  ep.bias_f32 = 0;
+  ep.act = GEMV_ACT_NONE;
+  return ep;
+}
+
+bool is_identity(const Epilogue &ep) {
+  return ep.alpha == 1.f && ep.bias == nullptr && ep.act == GEMV_ACT_NONE;
+}
+
+int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_t k, int dtype,
+           const gemv_config *forced, const Epilogue &ep, cudaStream_t stream) {
   int inj = g_inject.exchange(0);
   if (inj != 0) return inj;
-  int st = validate(B, a, c, n, k, dtype);
+  int st = validate_ld(B, ldb, a, c, n, k, dtype);
   if (st != GEMV_OK) return st;
   if (n == 0) return GEMV_OK;
 
@@ -449,15 +469,24 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
     return GEMV_ERR_DEVICE;
   }
   if (k == 0) {
-    // The empty sum: +0 in every output format is all-zero bits.
-    e = cudaMemsetAsync(c, 0, (size_t)n * out_elem_bytes(dtype), stream);
+    // The empty sum: +0 in every output format is all-zero bits; with an
+    // epilogue, its value on 0 (the second-pass kernel over no partials).
+    if (is_identity(ep)) {
+      e = cudaMemsetAsync(c, 0, (size_t)n * out_elem_bytes(dtype), stream);
+    } else {
+      ReduceKernel rk = lookup_reduce(dtype);
+      int64_t blocks = cdiv(n, kReduceThreads);
+      if (blocks > 65535) blocks = 65535;
+      rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(nullptr, c, n, 0, ep);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     gemv_config z{};
     t_last = z;
     t_has_last = true;
     return GEMV_OK;
   }
-  const bool aligned = (((uintptr_t)B & 15u) == 0) && (k % 8 == 0);
+  const bool aligned = (((uintptr_t)B & 15u) == 0) && (k % 8 == 0) && (ldb % 8 == 0);
   const int overlap = forced ? forced->overlap : GEMV_OVERLAP_NONE;
   if (overlap < GEMV_OVERLAP_NONE || overlap > GEMV_OVERLAP_PDL_PREFETCH_BA) return GEMV_ERR_CONFIG;
 
@@ -504,12 +533,14 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
   p.ws = ws;
   p.n = n;
   p.k = k;
+  p.ldb = ldb;
   p.kseg = cfg.k_segment;
   p.base_off = (int32_t)(((uintptr_t)B >> 1) & 7u);
   p.sg = cfg.grid_split;
   p.sw = cfg.warp_split;
   p.nrb = cfg.row_blocks;
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
+  p.ep = ep;
   p.flags = ((overlap >= GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
             ((overlap == GEMV_OVERLAP_PDL_PREFETCH_BA) ? kFlagPrefetchA : 0) |
             (cfg.l2_prefetch << kFlagL2Shift);
@@ -534,13 +565,18 @@ int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, 
     lc.blockDim = dim3(kReduceThreads);
     lc.dynamicSmemBytes = 0;
     const float *wsc = ws;
-    e = cudaLaunchKernelEx(&lc, rk, wsc, c, n, (int32_t)cfg.grid_split);
+    e = cudaLaunchKernelEx(&lc, rk, wsc, c, n, (int32_t)cfg.grid_split, ep);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   cfg.overlap = overlap;
   t_last = cfg;
   t_has_last = true;
   return GEMV_OK;
+}
+
+int run(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype, const gemv_config *forced,
+        cudaStream_t stream) {
+  return run_ld(B, k, a, c, n, k, dtype, forced, identity_epilogue(), stream);
 }
 
 }  // namespace
@@ -556,6 +592,26 @@ extern "C" int gemv(const void *B, const void *a, void *c, int64_t n, int64_t k,
 extern "C" int gemv_ex(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
                        const gemv_config *forced, cudaStream_t stream) {
   return run(B, a, c, n, k, dtype, forced, stream);
+}
+
+extern "C" int gemv_fused(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_t k, int dtype,
+                          const gemv_epilogue *epilogue, const gemv_config *config, cudaStream_t stream) {
+  Epilogue ep = identity_epilogue();
+  if (epilogue != nullptr) {
+    if (epilogue->activation < GEMV_ACT_NONE || epilogue->activation > GEMV_ACT_SILU) return GEMV_ERR_ARG;
+    if (epilogue->bias_dtype != GEMV_BIAS_INPUT_TYPE && epilogue->bias_dtype != GEMV_BIAS_F32) return GEMV_ERR_ARG;
+    ep.alpha = epilogue->alpha;
+    ep.beta = epilogue->beta;
+    ep.bias = epilogue->bias;
+    ep.bias_f32 = epilogue->bias_dtype == GEMV_BIAS_F32 ? 1 : 0;
+    ep.act = epilogue->activation;
+    if (ep.bias != nullptr && n > 0) {
+      const int be = ep.bias_f32 ? 4 : 2;
+      if ((uintptr_t)ep.bias % (uintptr_t)be != 0) return GEMV_ERR_ALIGN;
+      if (c != nullptr && overlaps(c, n * out_elem_bytes(dtype), ep.bias, n * be)) return GEMV_ERR_ALIAS;
+    }
+  }
+  return run_ld(B, ldb, a, c, n, k, dtype, config, ep, stream);
 }
 
 extern "C" int gemv_plan(int64_t n, int64_t k, int dtype, int b_aligned16, int sm_count,
@@ -783,6 +839,7 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
   p.ws = ws;
   p.n = n;
   p.k = k;
+  p.ldb = k;
   p.kseg = cfg.k_segment;
   p.base_off = (int32_t)(((uintptr_t)B >> 1) & 7u);
   p.sg = cfg.grid_split;
@@ -790,6 +847,7 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
   p.nrb = cfg.row_blocks;
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
   p.flags = 0;
+  p.ep = identity_epilogue();
   // Every (segment, row) partial is written by the first kernel before the
   // second reads it, so the scratch needs no clearing between calls.
   mk<<<cfg.ctas, cfg.warps_per_cta * 32, cfg.smem_bytes, stream>>>(p);
@@ -799,7 +857,7 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
     ReduceKernel rk = lookup_reduce(dtype);
     int64_t blocks = cdiv(n, kReduceThreads);
     if (blocks > 65535) blocks = 65535;
-    rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split);
+    rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split, identity_epilogue());
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
   }

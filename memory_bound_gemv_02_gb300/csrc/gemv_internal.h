@@ -6,6 +6,17 @@
 
 namespace gemvk {
 
+// Fused epilogue applied to each row total before the single rounding:
+// y = act(alpha * acc + beta * bias[row]) (bias optional, in the input type
+// or fp32).  alpha = 1, no bias and act = 0 leave acc unchanged.
+struct Epilogue {
+  float alpha;
+  float beta;
+  const void *bias;  // n elements or nullptr
+  int32_t bias_f32;  // 1: bias is fp32, 0: bias has the input type
+  int32_t act;       // 0 none, 1 relu, 2 sigmoid, 3 silu
+};
+
 // Launch parameters of the main streaming kernel (passed by value).
 struct Params {
   const uint16_t *B;  // n x k row-major, element (2-byte) aligned
@@ -14,6 +25,7 @@ struct Params {
   float *ws;          // fp32 partials ws[s * n + row], when grid_split > 1
   int64_t n;
   int64_t k;
+  int64_t ldb;        // row stride of B in elements (>= k)
   int64_t kseg;       // columns per k-segment
   int32_t base_off;   // (address of B / 2) mod 8: B's element offset within a 16-byte block
   int32_t sg;         // grid split (CTAs per row block)
@@ -21,11 +33,12 @@ struct Params {
   int32_t nrb;        // row blocks = gridDim.x / sg
   int32_t as_elems;   // staged a elements per CTA (multiple of 8, >= kseg + 24)
   int32_t flags;      // kFlagPrefetchB | kFlagPrefetchA | (L2 prefetch rounds << kFlagL2Shift)
+  Epilogue ep;
   // Tiles kernel: sw = S (warps per row, slices), nrb = C (CTAs per k-segment).
 };
 
 typedef void (*MainKernel)(Params);
-typedef void (*ReduceKernel)(const float *, void *, int64_t, int32_t);
+typedef void (*ReduceKernel)(const float *, void *, int64_t, int32_t, Epilogue);
 typedef void (*ProbeKernel)(const uint4 *, int64_t, uint32_t *);
 
 // Kernel lookup.  in16: 0 fp16, 1 bf16.  out_f32: 0 same as input, 1 fp32.

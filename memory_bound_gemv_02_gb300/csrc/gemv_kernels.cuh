@@ -42,6 +42,7 @@ struct F16 {
   static __device__ __forceinline__ uint16_t from_float(float x) {
     return __half_as_ushort(__float2half_rn(x));
   }
+  static __device__ __forceinline__ float to_float(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 };
 
 struct BF16 {
@@ -52,6 +53,7 @@ struct BF16 {
   static __device__ __forceinline__ uint16_t from_float(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
   }
+  static __device__ __forceinline__ float to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 };
 
 // --------------------------------------------------------------- memory --
@@ -199,14 +201,39 @@ __device__ __forceinline__ void stage_a(const Params &p, uint4 *as4, int64_t j0,
 
 // ---------------------------------------------------------------- output --
 
+// The fused epilogue on a row total, in fp32: y = act(alpha * v + beta *
+// bias[row]).  With alpha = 1, no bias and no activation it returns v
+// unchanged.  The activations call CUDA's expf.
+template <class T>
+__device__ __forceinline__ float apply_epilogue(const Epilogue &ep, int64_t row, float v) {
+  float y = ep.alpha * v;
+  if (ep.bias != nullptr) {
+    const float b = ep.bias_f32 ? static_cast<const float *>(ep.bias)[row]
+                                : T::to_float(static_cast<const uint16_t *>(ep.bias)[row]);
+    y = fmaf(ep.beta, b, y);
+  }
+  switch (ep.act) {
+    case 1: y = y > 0.f ? y : 0.f; break;                // relu
+    case 2: y = 1.f / (1.f + expf(-y)); break;           // sigmoid
+    case 3: y = y / (1.f + expf(-y)); break;             // silu: y * sigmoid(y)
+    default: break;
+  }
+  return y;
+}
+
+// Final store of a row (rounded once), or its fp32 partial under split-K
+// (the epilogue then runs in the second pass).
 template <class T, bool OUT_F32>
 __device__ __forceinline__ void store_out(const Params &p, int gs, int64_t row, float v) {
   if (p.sg > 1) {
     p.ws[(int64_t)gs * p.n + row] = v;
-  } else if (OUT_F32) {
-    static_cast<float *>(p.c)[row] = v;
+    return;
+  }
+  const float y = apply_epilogue<T>(p.ep, row, v);
+  if (OUT_F32) {
+    static_cast<float *>(p.c)[row] = y;
   } else {
-    static_cast<uint16_t *>(p.c)[row] = T::from_float(v);
+    static_cast<uint16_t *>(p.c)[row] = T::from_float(y);
   }
 }
 
@@ -220,8 +247,8 @@ __device__ __forceinline__ void rows_aligned(const Params &p, const uint4 *as4, 
                                              int64_t j0, int t0, int t1, int lane, float (&out)[R]) {
   // Called with i0 < r1.  Rows past r1 (only in the CTA's last group)
   // re-read row i0 and their sums are discarded.
-  const uint4 *b0 = reinterpret_cast<const uint4 *>(p.B + i0 * p.k + j0);
-  const int kv = (int)(p.k >> 3);  // row stride in 16-byte vectors
+  const uint4 *b0 = reinterpret_cast<const uint4 *>(p.B + i0 * p.ldb + j0);
+  const int kv = (int)(p.ldb >> 3);  // row stride in 16-byte vectors
   int roff[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) roff[r] = (i0 + r < r1) ? r * kv : 0;
@@ -297,7 +324,7 @@ template <class T, int U>
 __device__ __forceinline__ float row_general_dispatch(const Params &p, const uint4 *as4, int64_t i, int64_t j0,
                                                       int64_t len, int s, int sw, int lane) {
   const uint4 *bal = reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p.B) & ~(uintptr_t)15);
-  const int64_t e0 = (int64_t)p.base_off + i * p.k + j0;  // element index from the aligned base
+  const int64_t e0 = (int64_t)p.base_off + i * p.ldb + j0;  // element index from the aligned base
   const int64_t g0 = e0 >> 3;
   const int off = (int)(e0 & 7);
   const int nt = (int)((off + len + 7) >> 3);
@@ -387,17 +414,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_rows_kernel(Params p) {
 // Second pass of split-K: c[row] = sum over segments s = 0 .. sg-1 (in that
 // order) of ws[s * n + row], rounded once to the output type.
 template <class T, bool OUT_F32>
-__global__ void __launch_bounds__(256) gemv_splitk_reduce_kernel(const float *ws, void *c, int64_t n, int32_t sg) {
+__global__ void __launch_bounds__(256)
+    gemv_splitk_reduce_kernel(const float *ws, void *c, int64_t n, int32_t sg, Epilogue ep) {
   allow_dependents();
   wait_for_predecessor();  // the partials come from the kernel before
   for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < n;
        row += (int64_t)gridDim.x * blockDim.x) {
     float v = 0.f;
     for (int s = 0; s < sg; ++s) v += ws[(int64_t)s * n + row];
+    const float y = apply_epilogue<T>(ep, row, v);
     if (OUT_F32) {
-      static_cast<float *>(c)[row] = v;
+      static_cast<float *>(c)[row] = y;
     } else {
-      static_cast<uint16_t *>(c)[row] = T::from_float(v);
+      static_cast<uint16_t *>(c)[row] = T::from_float(y);
     }
   }
 }

@@ -10,7 +10,8 @@
 //    uses), instead of thousands of unrelated row streams spread over the
 //    matrix, and CTA loads differ by at most one row.
 //  * One code path for any alignment.  The rows of B start at element
-//    offset (base + i*k) mod 8 inside a 16-byte block, which depends only on
+//    offset (base + i*ldb) mod 8 inside a 16-byte block (ldb = the row
+//    stride, k unless the caller passes a padded one), which depends only on
 //    i mod 8.  CTAs are assigned one residue class of rows each, so every
 //    row a CTA reads has the same offset `off`: the CTA stages its k-segment
 //    of a shifted by `off` once, and row blocks then line up with staged
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   const int64_t len = (p.k - j0 < p.kseg) ? (p.k - j0) : p.kseg;
   // rows of this class: i = NCLS * j + cls, 0 <= j < nr
   const int64_t nr = (p.n > cls) ? (p.n - cls + NCLS - 1) / NCLS : 0;
-  const int off = ALIGNED ? 0 : (int)(((int64_t)p.base_off + j0 + (int64_t)cls * (p.k & 7)) & 7);
+  const int off = ALIGNED ? 0 : (int)(((int64_t)p.base_off + j0 + (int64_t)cls * (p.ldb & 7)) & 7);
   const int nt = (int)((off + len + 7) >> 3);
   const int last_hi = (int)(len + off - 8 * (int64_t)(nt - 1));
 
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       valid[r] = (mb + r) < nloc;
-      g0[r] = valid[r] ? (((int64_t)p.base_off + row_of(mb + r) * p.k + j0) >> 3) : 0;
+      g0[r] = valid[r] ? (((int64_t)p.base_off + row_of(mb + r) * p.ldb + j0) >> 3) : 0;
     }
   };
 
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     if (g < ngroups && lane < R && t1 > t0) {
       const int64_t m = g * RT + (int64_t)slot * R + lane;
       if (m < nloc) {
-        const int64_t gb = ((int64_t)p.base_off + row_of(m) * p.k + j0) >> 3;
+        const int64_t gb = ((int64_t)p.base_off + row_of(m) * p.ldb + j0) >> 3;
         prefetch_l2(bal + gb + t0, (uint32_t)(t1 - t0) * 16u);
       }
     }

@@ -32,6 +32,8 @@ _LIB = os.path.join(_HERE, "libgemv_ref.so")
 
 #: format codes of gemv_ref.c
 FMT = {"f16": 0, "bf16": 1, "f32": 2}
+#: activation codes of gemv_ref.c
+ACT = {"none": 0, "relu": 1, "sigmoid": 2, "silu": 3}
 
 _lock = threading.Lock()
 _default = None
@@ -75,6 +77,9 @@ class Oracle:
         lib.gemv_ref.restype = ctypes.c_int
         lib.gemv_ref_rows.argtypes = [vp, vp, i64, i64, ctypes.c_int, vp, i64, vp, vp]
         lib.gemv_ref_rows.restype = ctypes.c_int
+        lib.gemv_ref_epilogue.argtypes = [vp, vp, i64, ctypes.c_double, ctypes.c_double, vp, ctypes.c_int,
+                                          ctypes.c_int, vp, vp]
+        lib.gemv_ref_epilogue.restype = ctypes.c_int
         self.lib = lib
 
     def decode(self, bits, fmt: str) -> np.ndarray:
@@ -126,6 +131,29 @@ class Oracle:
         """Round oracle results to the output format's bit patterns."""
         return self.encode(c, out_fmt)
 
+    def gemv_ref_epilogue(self, c, s, alpha=1.0, beta=0.0, bias_bits=None, bias_fmt="f32",
+                          act: str = "none"):
+        """y = act(alpha * c + beta * bias) in binary64 and the tolerance scale
+        (|alpha| s + |beta bias|) * max slope of act.  ``bias_bits``: uint16
+        patterns of 'f16'/'bf16' or uint32 patterns of 'f32', or None."""
+        c = np.ascontiguousarray(c, dtype=np.float64)
+        s = np.ascontiguousarray(s, dtype=np.float64)
+        n = c.size
+        y = np.zeros(n, dtype=np.float64)
+        scale = np.zeros(n, dtype=np.float64)
+        bptr = None
+        if bias_bits is not None:
+            bias_bits = np.ascontiguousarray(bias_bits)
+            want = np.uint32 if bias_fmt == "f32" else np.uint16
+            if bias_bits.dtype != want or bias_bits.size != n:
+                raise TypeError("bias bit patterns of the wrong type or size")
+            bptr = _ptr(bias_bits)
+        rc = self.lib.gemv_ref_epilogue(_ptr(c), _ptr(s), n, float(alpha), float(beta), bptr, FMT[bias_fmt],
+                                        ACT[act], _ptr(y), _ptr(scale))
+        if rc != 0:
+            raise ValueError("gemv_ref_epilogue rejected its arguments")
+        return y, scale
+
 
 def default() -> Oracle:
     """The oracle built from this directory's ``gemv_ref.c``."""
@@ -154,3 +182,7 @@ def gemv_ref_rows(B_bits, a_bits, fmt, rows):
 
 def round_out(c, out_fmt):
     return default().round_out(c, out_fmt)
+
+
+def gemv_ref_epilogue(c, s, alpha=1.0, beta=0.0, bias_bits=None, bias_fmt="f32", act="none"):
+    return default().gemv_ref_epilogue(c, s, alpha, beta, bias_bits, bias_fmt, act)

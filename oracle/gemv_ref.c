@@ -28,6 +28,12 @@
  * Compiled with -O2 -ffp-contract=off and without -ffast-math, so that every
  * product and every sum is one correctly rounded binary64 operation.
  *
+ * The fused epilogue (the TileLang optimization guide, "Epilogue Fusion":
+ * scaling, bias and activation applied to the result before it is stored)
+ * is gemv_ref_epilogue(): y_i = act(alpha * c_i + beta * bias_i) in binary64
+ * with act = identity, relu (max(y, 0), 0 for NaN), sigmoid 1/(1 + e^-y) or
+ * silu y/(1 + e^-y), exp from the C library.
+ *
  * Pins (tests/test_oracle.py): exhaustive decode of all 2^16 patterns of both
  * formats against torch's CPU casts; encode against numpy/torch casts and
  * constructed halfway and overflow cases; B = ones, a = ones gives k exactly;
@@ -185,6 +191,56 @@ int gemv_ref_rows(const uint16_t *B, const uint16_t *a, int64_t n, int64_t k, in
     if (rows[r] < 0 || rows[r] >= n) return -1;
     int rc = gemv_ref(B + rows[r] * k, a, 1, k, in_fmt, c + r, s + r);
     if (rc != 0) return rc;
+  }
+  return 0;
+}
+
+/* Activation codes (the same numbering as the library's, written here
+ * independently). */
+#define REF_ACT_NONE 0
+#define REF_ACT_RELU 1
+#define REF_ACT_SIGMOID 2
+#define REF_ACT_SILU 3
+
+static double ref_activation(double y, int act) {
+  switch (act) {
+    case REF_ACT_RELU: return y > 0.0 ? y : 0.0;
+    case REF_ACT_SIGMOID: return 1.0 / (1.0 + exp(-y));
+    case REF_ACT_SILU: return y / (1.0 + exp(-y));
+    default: return y;
+  }
+}
+
+/* Largest slope of each activation (bounds how an error in its argument
+ * propagates): 1 for identity and relu, 1/4 for sigmoid, < 1.1 for silu. */
+static double ref_activation_slope(int act) {
+  switch (act) {
+    case REF_ACT_SIGMOID: return 0.25;
+    case REF_ACT_SILU: return 1.1;
+    default: return 1.0;
+  }
+}
+
+/*
+ * y_i = act(alpha * c_i + beta * bias_i) for i < n, in binary64.  bias holds
+ * n bit patterns of bias_fmt (REF_F16 or REF_BF16: uint16, REF_F32: uint32)
+ * or is NULL (no bias).  scale_i = (|alpha| s_i + |beta bias_i|) * slope(act)
+ * is the size against which the fp32-output tolerance is stated (s_i from
+ * gemv_ref).  Returns 0, or -1 for a bad argument.
+ */
+int gemv_ref_epilogue(const double *c, const double *s, int64_t n, double alpha, double beta, const void *bias,
+                      int bias_fmt, int act, double *y, double *scale) {
+  if (n < 0 || act < REF_ACT_NONE || act > REF_ACT_SILU) return -1;
+  if (bias != NULL && bias_fmt != REF_F16 && bias_fmt != REF_BF16 && bias_fmt != REF_F32) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    double b = 0.0;
+    if (bias != NULL) {
+      uint32_t bits = (bias_fmt == REF_F32) ? ((const uint32_t *)bias)[i] : ((const uint16_t *)bias)[i];
+      b = ref_decode_bits(bits, bias_fmt);
+    }
+    double pre = alpha * c[i] + beta * b;
+    y[i] = ref_activation(pre, act);
+    scale[i] = (fabs(alpha) * s[i] + fabs(beta * b)) * ref_activation_slope(act);
   }
   return 0;
 }

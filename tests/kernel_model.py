@@ -22,10 +22,13 @@ def _row_range(rbk, n, nrb):
     return r0, r0 + q + (1 if rbk < rem else 0)
 
 
-def replay(n, k, cfg, base_off=0):
-    """Return a dict of findings; raises AssertionError on any violation."""
+def replay(n, k, cfg, base_off=0, ldb=None):
+    """Return a dict of findings; raises AssertionError on any violation.
+    ``ldb``: row stride of B in elements (default k)."""
+    ldb = k if ldb is None else ldb
     if cfg["variant"] == 3:
-        return replay_tiles(n, k, cfg, base_off)
+        return replay_tiles(n, k, cfg, base_off, ldb)
+    assert ldb == k, "row-per-warp replay models ldb == k only"
     W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
     nrb, kseg, variant, ctas = cfg["row_blocks"], cfg["k_segment"], cfg["variant"], cfg["ctas"]
     assert ctas == nrb * Sg and W % Sw == 0
@@ -106,11 +109,13 @@ def replay(n, k, cfg, base_off=0):
     return {"ctas": ctas}
 
 
-def replay_tiles(n, k, cfg, base_off=0):
-    """The same checks for ``gemv_tiles_kernel``."""
+def replay_tiles(n, k, cfg, base_off=0, ldb=None):
+    """The same checks for ``gemv_tiles_kernel`` (row i of B starts at
+    element i * ldb)."""
+    ldb = k if ldb is None else ldb
     W, R, S, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
     C, kseg, U, ctas = cfg["row_blocks"], cfg["k_segment"], cfg["unroll"], cfg["ctas"]
-    aligned = base_off == 0 and k % 8 == 0
+    aligned = base_off == 0 and k % 8 == 0 and ldb % 8 == 0
     NCLS = 1 if aligned else 8
     assert ctas == C * Sg and W % S == 0 and C % NCLS == 0 and C >= NCLS
     assert (R, U) in ((1, 8), (1, 4), (2, 4), (4, 2))
@@ -120,7 +125,7 @@ def replay_tiles(n, k, cfg, base_off=0):
     if S > 1:
         assert 1 + slots - 1 <= 15  # named barrier ids 1..slots
     cover = np.zeros((n, k), dtype=np.int32)
-    nblocks = -(-(base_off + n * k) // 8)
+    nblocks = -(-(base_off + (n - 1) * ldb + k) // 8)  # blocks holding any byte of B's rows
     ws_rows = set()
     Cq = C // NCLS
     for cta in range(ctas):
@@ -130,7 +135,7 @@ def replay_tiles(n, k, cfg, base_off=0):
         seglen = min(k - j0, kseg)
         assert seglen >= 1
         nr = (n - cls + NCLS - 1) // NCLS if n > cls else 0
-        off = 0 if aligned else (base_off + j0 + cls * (k & 7)) & 7
+        off = 0 if aligned else (base_off + j0 + cls * (ldb & 7)) & 7
         nt = (off + seglen + 7) >> 3
         last_hi = seglen + off - 8 * (nt - 1)
         assert 1 <= last_hi <= 8
@@ -158,7 +163,7 @@ def replay_tiles(n, k, cfg, base_off=0):
                     assert j < nr
                     i = NCLS * j + cls
                     assert i < n
-                    e0 = base_off + i * k + j0
+                    e0 = base_off + i * ldb + j0
                     assert (e0 & 7) == off, "row offset differs inside a CTA"
                     g0 = e0 >> 3
                     if t1 <= t0:
@@ -173,7 +178,7 @@ def replay_tiles(n, k, cfg, base_off=0):
                     else:
                         valid = ((tt > 0) | (p >= off)) & ((tt < nt - 1) | (p < last_hi))
                     elem = 8 * blk[:, None] + p - base_off
-                    col_B = elem - i * k - j0
+                    col_B = elem - i * ldb - j0
                     col_stage = stage_col[8 * tt + p]
                     assert (col_B[valid] == col_stage[valid]).all()
                     assert (col_B[valid] >= 0).all() and (col_B[valid] < seglen).all()

@@ -96,3 +96,25 @@ def test_config_struct_layout_matches_header(gemv_lib):
     # int32 x 8, int64, int32 x 2, int32[4]  ->  8*4 + 8 + 2*4 + 16 = 64 bytes
     assert ctypes.sizeof(gemv_lib.GemvConfig) == 64
     assert gemv_lib.GemvConfig.k_segment.offset == 32
+
+
+def test_fused_argument_validation_without_gpu(gemv_lib):
+    L = gemv_lib.lib()
+    g = gemv_lib
+    ep = g.GemvEpilogue()
+    ep.alpha, ep.beta = 1.0, 1.0
+    call = lambda B, ldb, a, c, n, k, dt, e: L.gemv_fused(B, ldb, a, c, n, k, dt, e, None, None)
+    assert call(B_ADDR, 7, A_ADDR, C_ADDR, 4, 8, 0, None) == g.GEMV_ERR_ARG      # ldb < k
+    ep.activation = 9
+    assert call(B_ADDR, 8, A_ADDR, C_ADDR, 4, 8, 0, ctypes.byref(ep)) == g.GEMV_ERR_ARG
+    ep.activation = g.GEMV_ACT_SILU
+    ep.bias_dtype = 5
+    assert call(B_ADDR, 8, A_ADDR, C_ADDR, 4, 8, 0, ctypes.byref(ep)) == g.GEMV_ERR_ARG
+    ep.bias_dtype = g.GEMV_BIAS_F32
+    ep.bias = C_ADDR + 0x1002  # fp32 bias must be 4-byte aligned
+    assert call(B_ADDR, 8, A_ADDR, C_ADDR, 4, 8, 0, ctypes.byref(ep)) == g.GEMV_ERR_ALIGN
+    ep.bias = C_ADDR + 4  # overlaps c (4 fp16 outputs = 8 bytes)
+    assert call(B_ADDR, 8, A_ADDR, C_ADDR, 4, 8, 0, ctypes.byref(ep)) == g.GEMV_ERR_ALIAS
+    # c inside a padded B: rows of 8 elements with stride 64 span (3*64 + 8) * 2 bytes
+    assert call(B_ADDR, 64, A_ADDR, B_ADDR + 300, 4, 8, 0, None) == g.GEMV_ERR_ALIAS
+    assert call(B_ADDR, 64, A_ADDR, B_ADDR + 400, 4, 8, 0, None) != g.GEMV_ERR_ALIAS

@@ -306,3 +306,43 @@ def test_ulp_helper():
         [2.0 ** -10, 2.0 ** -10, 2.0 ** -9, 2.0 ** -24]
     assert parity_rules.ulp(np.array([7168.0]), "bf16")[0] == 32.0
     assert math.isclose(parity_rules.ulp(np.array([1.0]), "f32")[0], 2.0 ** -23)
+
+
+# ------------------------------------------------------------- epilogue --
+
+def test_epilogue_closed_forms():
+    """Values the activations' definitions fix exactly (or to one rounding)."""
+    ln3 = math.log(3.0)
+    c = np.array([0.0, ln3, -ln3, 2.5, -2.5, 0.0])
+    s = np.abs(c)
+    y, _ = oracle.gemv_ref_epilogue(c, s, act="sigmoid")
+    assert y[0] == 0.5
+    assert abs(y[1] - 0.75) <= 2 ** -52 and abs(y[2] - 0.25) <= 2 ** -53
+    assert abs(y[3] + y[4] - 1.0) <= 2 ** -52  # sigmoid(x) + sigmoid(-x) = 1
+    y, _ = oracle.gemv_ref_epilogue(c, s, act="silu")
+    assert y[0] == 0.0 and abs(y[1] - 0.75 * ln3) <= 2 ** -51
+    assert abs((y[3] - y[4]) - 2.5) <= 2 ** -50  # silu(x) - silu(-x) = x
+    y, _ = oracle.gemv_ref_epilogue(c, s, act="relu")
+    assert y.tolist() == [0.0, ln3, 0.0, 2.5, 0.0, 0.0]
+    nan_y, _ = oracle.gemv_ref_epilogue(np.array([np.nan]), np.array([0.0]), act="relu")
+    assert nan_y[0] == 0.0  # max(NaN, 0) taken as 0
+
+
+def test_epilogue_scale_and_bias_exact():
+    """Identity activation: y = alpha c + beta bias exactly for small dyadic
+    values, with the bias decoded from each format's bit patterns."""
+    c = np.array([1.0, -2.0, 0.5, 3.0])
+    s = np.array([4.0, 2.0, 1.0, 3.0])
+    bias = np.array([0.25, -1.0, 8.0, 0.0])
+    for fmt, tdt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        bits = inputs.to_bits(torch.tensor(bias, dtype=tdt))
+        y, scale = oracle.gemv_ref_epilogue(c, s, alpha=2.0, beta=-0.5, bias_bits=bits, bias_fmt=fmt)
+        assert y.tolist() == (2.0 * c - 0.5 * bias).tolist()
+        assert scale.tolist() == (2.0 * s + 0.5 * np.abs(bias)).tolist()
+    bits32 = bias.astype(np.float32).view(np.uint32)
+    y, _ = oracle.gemv_ref_epilogue(c, s, alpha=1.0, beta=1.0, bias_bits=bits32, bias_fmt="f32")
+    assert y.tolist() == (c + bias).tolist()
+    y, scale = oracle.gemv_ref_epilogue(c, s)  # defaults: identity
+    assert y.tolist() == c.tolist() and scale.tolist() == s.tolist()
+    _, scale = oracle.gemv_ref_epilogue(c, s, act="sigmoid")
+    assert scale.tolist() == (0.25 * s).tolist()

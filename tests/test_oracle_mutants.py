@@ -9,6 +9,7 @@ must pass all of them.  CPU only; the mutants never touch a GPU.
 """
 from __future__ import annotations
 
+import math
 import os
 from fractions import Fraction
 
@@ -33,6 +34,10 @@ MUTANTS = {
     "ties_away": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
     "abs_sum_signed": ("acc_abs += fabs(p);", "acc_abs += p;"),
     "bf16_as_f16": ("if (fmt == REF_F16) {", "if (fmt == REF_F16 || fmt == REF_BF16) {"),
+    "sigmoid_sign": ("case REF_ACT_SIGMOID: return 1.0 / (1.0 + exp(-y));", "case REF_ACT_SIGMOID: return 1.0 / (1.0 + exp(y));"),
+    "silu_as_sigmoid": ("case REF_ACT_SILU: return y / (1.0 + exp(-y));", "case REF_ACT_SILU: return 1.0 / (1.0 + exp(-y));"),
+    "bias_sign": ("double pre = alpha * c[i] + beta * b;", "double pre = alpha * c[i] - beta * b;"),
+    "relu_leaky": ("case REF_ACT_RELU: return y > 0.0 ? y : 0.0;", "case REF_ACT_RELU: return y > 0.0 ? y : 0.01 * y;"),
 }
 
 
@@ -91,7 +96,22 @@ def _check_bruteforce(o):
                 assert abs(Fraction(s[i]) - S) <= Fraction(7, 2 ** 53) * S
 
 
-PINS = [_check_decode, _check_encode, _check_closed_forms, _check_bruteforce]
+def _check_epilogue(o):
+    ln3 = math.log(3.0)
+    c = np.array([0.0, ln3, -2.0, 2.5])
+    s = np.abs(c)
+    y, _ = o.gemv_ref_epilogue(c, s, act="sigmoid")
+    assert y[0] == 0.5 and abs(y[1] - 0.75) <= 2 ** -52
+    y, _ = o.gemv_ref_epilogue(c, s, act="silu")
+    assert abs(y[1] - 0.75 * ln3) <= 2 ** -51
+    y, _ = o.gemv_ref_epilogue(c, s, act="relu")
+    assert y.tolist() == [0.0, ln3, 0.0, 2.5]
+    bits = inputs.to_bits(torch.tensor([1.0, 2.0, 3.0, 4.0], dtype=torch.float16))
+    y, _ = o.gemv_ref_epilogue(c, s, alpha=2.0, beta=0.5, bias_bits=bits, bias_fmt="f16")
+    assert y.tolist() == (2.0 * c + 0.5 * np.array([1.0, 2.0, 3.0, 4.0])).tolist()
+
+
+PINS = [_check_decode, _check_encode, _check_closed_forms, _check_bruteforce, _check_epilogue]
 
 
 def _failures(o):

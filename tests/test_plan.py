@@ -182,3 +182,20 @@ def test_shifted_staging_model(off, j0, seglen, k):
         if off <= x < off + seglen:
             want[x] = a[j0 + x - off]
     assert (got == want).all()
+
+
+@pytest.mark.parametrize("n,k,ldb", [(5, 17, 24), (9, 64, 72), (9, 64, 67), (33, 100, 100), (17, 7, 8), (3, 4099, 5000),
+                                     (40, 256, 264), (7, 1000, 1003)])
+@pytest.mark.parametrize("base_off", [0, 3])
+@pytest.mark.parametrize("forced", [None, {"warp_split": 2}, {"grid_split": 3}, {"rows_per_warp": 2, "unroll": 4}])
+def test_tiles_index_replay_strided(gemv_lib, n, k, ldb, base_off, forced):
+    """Row-strided B (ldb >= k): rows start at i * ldb; aligned only when the
+    base, k and ldb all allow it."""
+    cfg_in = dict(forced or {})
+    cfg_in["variant"] = 3
+    aligned = base_off == 0 and ldb % 8 == 0
+    try:
+        cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config=cfg_in)
+    except gemv_lib.GemvError:
+        pytest.skip("configuration not valid for this shape")
+    kernel_model.replay(n, k, cfg, base_off=base_off, ldb=ldb)
