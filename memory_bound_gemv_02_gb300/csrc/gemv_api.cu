@@ -359,11 +359,11 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
   return GEMV_OK;
 }
 
-MainKernel lookup_main(int dtype, const gemv_config &c, bool aligned) {
+MainKernel lookup_main(int dtype, const gemv_config &c, bool aligned, bool epi = false) {
   const int of = dtype >= 2 ? 1 : 0;
   if (c.variant == GEMV_VARIANT_TILES) {
-    return (dtype & 1) ? tiles_kernel_bf16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll)
-                       : tiles_kernel_f16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll);
+    return (dtype & 1) ? tiles_kernel_bf16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll, epi ? 1 : 0)
+                       : tiles_kernel_f16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll, epi ? 1 : 0);
   }
   return (dtype & 1) ? main_kernel_bf16(of, c.variant, c.rows_per_warp)
                      : main_kernel_f16(of, c.variant, c.rows_per_warp);
@@ -516,7 +516,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
       }
     }
     if (cfg.smem_bytes > di.max_smem_optin) return GEMV_ERR_CONFIG;
-    mk = lookup_main(dtype, cfg, aligned);
+    mk = lookup_main(dtype, cfg, aligned, !is_identity(ep));
     if (mk == nullptr) return GEMV_ERR_CONFIG;
     e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -543,7 +543,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   p.ep = ep;
   p.flags = ((overlap >= GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
             ((overlap == GEMV_OVERLAP_PDL_PREFETCH_BA) ? kFlagPrefetchA : 0) |
-            (cfg.l2_prefetch << kFlagL2Shift);
+            (is_identity(ep) ? 0 : kFlagEpilogue) | (cfg.l2_prefetch << kFlagL2Shift);
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

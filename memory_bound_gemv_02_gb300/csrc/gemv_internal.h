@@ -32,7 +32,7 @@ struct Params {
   int32_t sw;         // warp split (warps per row inside a CTA)
   int32_t nrb;        // row blocks = gridDim.x / sg
   int32_t as_elems;   // staged a elements per CTA (multiple of 8, >= kseg + 24)
-  int32_t flags;      // kFlagPrefetchB | kFlagPrefetchA | (L2 prefetch rounds << kFlagL2Shift)
+  int32_t flags;      // kFlag* bits | (L2 prefetch rounds << kFlagL2Shift)
   Epilogue ep;
   // Tiles kernel: sw = S (warps per row, slices), nrb = C (CTAs per k-segment).
 };
@@ -48,8 +48,9 @@ MainKernel main_kernel_f16(int out_f32, int variant, int R);
 MainKernel main_kernel_bf16(int out_f32, int variant, int R);
 // Tiles kernel: aligned = 1 for the single-class fast path; (R, U) in
 // {(1,8), (1,4), (2,4), (4,2)}.
-MainKernel tiles_kernel_f16(int out_f32, int aligned, int R, int U);
-MainKernel tiles_kernel_bf16(int out_f32, int aligned, int R, int U);
+// epi = 1 selects the copy built with the fused epilogue.
+MainKernel tiles_kernel_f16(int out_f32, int aligned, int R, int U, int epi);
+MainKernel tiles_kernel_bf16(int out_f32, int aligned, int R, int U, int epi);
 ReduceKernel reduce_kernel_f16(int out_f32);
 ReduceKernel reduce_kernel_bf16(int out_f32);
 ProbeKernel probe_kernel();
@@ -60,6 +61,7 @@ inline int unroll_for_rows(int R) { return R == 1 ? 8 : (R == 2 ? 4 : 2); }
 constexpr int kMaxThreads = 512;  // launch bound of the main kernel
 constexpr int kFlagPrefetchB = 1;
 constexpr int kFlagL2Shift = 1;  // 2 bits: tile rounds of bulk L2 prefetch ahead
-constexpr int kFlagPrefetchA = 8;  // stage a before waiting on the predecessor
+constexpr int kFlagPrefetchA = 8;   // stage a before waiting on the predecessor
+constexpr int kFlagEpilogue = 16;   // the fused epilogue is not the identity
 
 }  // namespace gemvk

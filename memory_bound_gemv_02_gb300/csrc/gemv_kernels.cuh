@@ -222,14 +222,19 @@ __device__ __forceinline__ float apply_epilogue(const Epilogue &ep, int64_t row,
 }
 
 // Final store of a row (rounded once), or its fp32 partial under split-K
-// (the epilogue then runs in the second pass).
-template <class T, bool OUT_F32>
+// (the epilogue then runs in the second pass).  EPI: the kernel was built
+// with the fused epilogue; plain GEMVs launch the copy without it, so their
+// streaming loop carries none of its code.
+template <class T, bool OUT_F32, bool EPI = true>
 __device__ __forceinline__ void store_out(const Params &p, int gs, int64_t row, float v) {
   if (p.sg > 1) {
     p.ws[(int64_t)gs * p.n + row] = v;
     return;
   }
-  const float y = apply_epilogue<T>(p.ep, row, v);
+  float y = v;
+  if constexpr (EPI) {
+    if (p.flags & kFlagEpilogue) y = apply_epilogue<T>(p.ep, row, v);
+  }
   if (OUT_F32) {
     static_cast<float *>(p.c)[row] = y;
   } else {

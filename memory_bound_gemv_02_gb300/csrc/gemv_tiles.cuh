@@ -144,7 +144,7 @@ __device__ __forceinline__ float tile_redo(const uint4 *bal, const uint4 *as4, i
 // Grid: blockIdx.x = c * sg + gs, c in [0, C) with C = p.nrb.  ALIGNED
 // (k % 8 == 0 and B 16-byte aligned) uses one row class; otherwise 8 classes
 // (C must be a multiple of 8), CTA c serving class c % 8.
-template <class T, bool OUT_F32, int U, int R, bool ALIGNED>
+template <class T, bool OUT_F32, int U, int R, bool ALIGNED, bool EPI>
 __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   extern __shared__ __align__(16) uint4 smem4[];
   uint4 *as4 = smem4;
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
       if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
-          if (valid[r]) store_out<T, OUT_F32>(p, gs, row_of(mb + r), v[r]);
+          if (valid[r]) store_out<T, OUT_F32, EPI>(p, gs, row_of(mb + r), v[r]);
       }
     } else {
       float *pb = ps + buf * (W * R);
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
         if (m < nloc) {
           float sum = 0.f;
           for (int s2 = 0; s2 < S; ++s2) sum += pb[(slot * R + lane) * S + s2];
-          store_out<T, OUT_F32>(p, gs, row_of(m), sum);
+          store_out<T, OUT_F32, EPI>(p, gs, row_of(m), sum);
         }
       }
       buf ^= 1;
@@ -286,21 +286,25 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
 }  // namespace gemvk
 
 // Instantiations of the tiles kernel for one input type: (U, R) in
-// {(8,1), (4,1), (4,2), (2,4)}, aligned or not, output same type or fp32.
-#define GEMV_TILES_CASES(T, OF, AL)                                     \
-  if (U == 8 && R == 1) return gemv_tiles_kernel<T, OF, 8, 1, AL>;      \
-  if (U == 4 && R == 1) return gemv_tiles_kernel<T, OF, 4, 1, AL>;      \
-  if (U == 4 && R == 2) return gemv_tiles_kernel<T, OF, 4, 2, AL>;      \
-  if (U == 2 && R == 4) return gemv_tiles_kernel<T, OF, 2, 4, AL>;
+// {(8,1), (4,1), (4,2), (2,4)}, aligned or not, output same type or fp32,
+// with or without the fused epilogue.
+#define GEMV_TILES_CASES(T, OF, AL, EP)                                     \
+  if (U == 8 && R == 1) return gemv_tiles_kernel<T, OF, 8, 1, AL, EP>;      \
+  if (U == 4 && R == 1) return gemv_tiles_kernel<T, OF, 4, 1, AL, EP>;      \
+  if (U == 4 && R == 2) return gemv_tiles_kernel<T, OF, 4, 2, AL, EP>;      \
+  if (U == 2 && R == 4) return gemv_tiles_kernel<T, OF, 2, 4, AL, EP>;
 
-#define GEMV_DEFINE_TILES_TABLE(T, SUFFIX)                                                  \
-  namespace gemvk {                                                                         \
-  MainKernel tiles_kernel_##SUFFIX(int out_f32, int aligned, int R, int U) {                \
-    if (out_f32) {                                                                          \
-      if (aligned) { GEMV_TILES_CASES(T, true, true) } else { GEMV_TILES_CASES(T, true, false) } \
-    } else {                                                                                \
-      if (aligned) { GEMV_TILES_CASES(T, false, true) } else { GEMV_TILES_CASES(T, false, false) } \
-    }                                                                                       \
-    return nullptr;                                                                         \
-  }                                                                                         \
+#define GEMV_TILES_BY_ALIGN(T, OF, EP)                                       \
+  if (aligned) { GEMV_TILES_CASES(T, OF, true, EP) } else { GEMV_TILES_CASES(T, OF, false, EP) }
+
+#define GEMV_DEFINE_TILES_TABLE(T, SUFFIX)                                             \
+  namespace gemvk {                                                                    \
+  MainKernel tiles_kernel_##SUFFIX(int out_f32, int aligned, int R, int U, int epi) {  \
+    if (out_f32) {                                                                     \
+      if (epi) { GEMV_TILES_BY_ALIGN(T, true, true) } else { GEMV_TILES_BY_ALIGN(T, true, false) } \
+    } else {                                                                           \
+      if (epi) { GEMV_TILES_BY_ALIGN(T, false, true) } else { GEMV_TILES_BY_ALIGN(T, false, false) } \
+    }                                                                                  \
+    return nullptr;                                                                    \
+  }                                                                                    \
   }
