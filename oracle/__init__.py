@@ -80,6 +80,9 @@ class Oracle:
         lib.gemv_ref_epilogue.argtypes = [vp, vp, i64, ctypes.c_double, ctypes.c_double, vp, ctypes.c_int,
                                           ctypes.c_int, vp, vp]
         lib.gemv_ref_epilogue.restype = ctypes.c_int
+        lib.gla_ref_decode.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_double, ctypes.c_int,
+                                       vp, vp, vp, vp]
+        lib.gla_ref_decode.restype = ctypes.c_int
         self.lib = lib
 
     def decode(self, bits, fmt: str) -> np.ndarray:
@@ -155,6 +158,29 @@ class Oracle:
         return y, scale
 
 
+    def gla_ref_decode(self, q, k, v, gk, S, scale: float, fmt: str):
+        """One GLA decode step for bh heads.  Bit-pattern arrays of ``fmt``
+        ('f16'/'bf16': uint16, 'f32': uint32): q, k, gk (bh, dk), v (bh, dv),
+        S (bh, dk, dv).  Returns binary64 (S_new, o, S_scale, o_scale)."""
+        want = np.uint32 if fmt == "f32" else np.uint16
+        arrs = [np.ascontiguousarray(x) for x in (q, k, v, gk, S)]
+        if any(x.dtype != want for x in arrs):
+            raise TypeError(f"expected {want.__name__} bit patterns for {fmt}")
+        q, k, v, gk, S = arrs
+        bh, dk, dv = S.shape
+        if q.shape != (bh, dk) or k.shape != (bh, dk) or gk.shape != (bh, dk) or v.shape != (bh, dv):
+            raise ValueError("shape mismatch")
+        S_new = np.zeros((bh, dk, dv))
+        ss = np.zeros((bh, dk, dv))
+        o = np.zeros((bh, dv))
+        os_ = np.zeros((bh, dv))
+        rc = self.lib.gla_ref_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(gk), _ptr(S), bh, dk, dv, float(scale),
+                                     FMT[fmt], _ptr(S_new), _ptr(o), _ptr(ss), _ptr(os_))
+        if rc != 0:
+            raise ValueError("gla_ref_decode rejected its arguments")
+        return S_new, o, ss, os_
+
+
 def default() -> Oracle:
     """The oracle built from this directory's ``gemv_ref.c``."""
     global _default
@@ -186,3 +212,7 @@ def round_out(c, out_fmt):
 
 def gemv_ref_epilogue(c, s, alpha=1.0, beta=0.0, bias_bits=None, bias_fmt="f32", act="none"):
     return default().gemv_ref_epilogue(c, s, alpha, beta, bias_bits, bias_fmt, act)
+
+
+def gla_ref_decode(q, k, v, gk, S, scale, fmt):
+    return default().gla_ref_decode(q, k, v, gk, S, scale, fmt)

@@ -34,6 +34,9 @@
  * with act = identity, relu (max(y, 0), 0 for NaN), sigmoid 1/(1 + e^-y) or
  * silu y/(1 + e^-y), exp from the C library.
  *
+ * gla_ref_decode() is one step of the gated-linear-attention recurrence
+ * (Case D "Background"), written out the same way.
+ *
  * Pins (tests/test_oracle.py): exhaustive decode of all 2^16 patterns of both
  * formats against torch's CPU casts; encode against numpy/torch casts and
  * constructed halfway and overflow cases; B = ones, a = ones gives k exactly;
@@ -241,6 +244,52 @@ int gemv_ref_epilogue(const double *c, const double *s, int64_t n, double alpha,
     double pre = alpha * c[i] + beta * b;
     y[i] = ref_activation(pre, act);
     scale[i] = (fabs(alpha) * s[i] + fabs(beta * b)) * ref_activation_slope(act);
+  }
+  return 0;
+}
+
+/*
+ * One decode step of gated linear attention (TileLang Case Studies, Case D
+ * "Background"), for bh independent heads:
+ *
+ *     S_new[i, j] = exp(gk[i]) * S[i, j] + k[i] * v[j]      (i < dk, j < dv)
+ *     o[j]        = scale * sum_{i<dk} q[i] * S_new[i, j]
+ *
+ * Layout per head h: q, k, gk at h*dk, v and o at h*dv, S and S_new at
+ * h*dk*dv (row i, column j at i*dv + j).  Inputs are bit patterns of fmt
+ * (REF_F16, REF_BF16 or REF_F32; uint16 or uint32 arrays), decoded from the
+ * format definitions; everything is computed in binary64, S_new before any
+ * rounding feeds o.  Outputs: S_new and o in binary64, plus the tolerance
+ * scales ss[h,i,j] = |exp(gk[i]) S[i,j]| + |k[i] v[j]| and
+ * os[h,j] = |scale| * sum_i |q[i] S_new[i,j]|.  Returns 0, or -1.
+ */
+static double ref_load(const void *p, int64_t idx, int fmt) {
+  uint32_t bits = (fmt == REF_F32) ? ((const uint32_t *)p)[idx] : ((const uint16_t *)p)[idx];
+  return ref_decode_bits(bits, fmt);
+}
+
+int gla_ref_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, int64_t bh,
+                   int64_t dk, int64_t dv, double scale, int fmt, double *S_new, double *o, double *ss,
+                   double *os) {
+  if (bh < 0 || dk < 0 || dv < 0) return -1;
+  if (fmt != REF_F16 && fmt != REF_BF16 && fmt != REF_F32) return -1;
+  for (int64_t h = 0; h < bh; ++h) {
+    for (int64_t j = 0; j < dv; ++j) {
+      double acc = 0.0, acc_abs = 0.0;
+      for (int64_t i = 0; i < dk; ++i) {
+        const double decay = exp(ref_load(gk, h * dk + i, fmt));
+        const double sij = ref_load(S, (h * dk + i) * dv + j, fmt);
+        const double kv = ref_load(k, h * dk + i, fmt) * ref_load(v, h * dv + j, fmt);
+        const double sn = decay * sij + kv;
+        S_new[(h * dk + i) * dv + j] = sn;
+        ss[(h * dk + i) * dv + j] = fabs(decay * sij) + fabs(kv);
+        const double qi = ref_load(q, h * dk + i, fmt);
+        acc += qi * sn;
+        acc_abs += fabs(qi * sn);
+      }
+      o[h * dv + j] = scale * acc;
+      os[h * dv + j] = fabs(scale) * acc_abs;
+    }
   }
   return 0;
 }

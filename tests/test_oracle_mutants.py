@@ -38,6 +38,10 @@ MUTANTS = {
     "silu_as_sigmoid": ("case REF_ACT_SILU: return y / (1.0 + exp(-y));", "case REF_ACT_SILU: return 1.0 / (1.0 + exp(-y));"),
     "bias_sign": ("double pre = alpha * c[i] + beta * b;", "double pre = alpha * c[i] - beta * b;"),
     "relu_leaky": ("case REF_ACT_RELU: return y > 0.0 ? y : 0.0;", "case REF_ACT_RELU: return y > 0.0 ? y : 0.01 * y;"),
+    "gla_decay_on_kv": ("const double sn = decay * sij + kv;", "const double sn = sij + decay * kv;"),
+    "gla_no_scale": ("o[h * dv + j] = scale * acc;", "o[h * dv + j] = acc;"),
+    "gla_transposed_state": ("ref_load(S, (h * dk + i) * dv + j, fmt)", "ref_load(S, (h * dv + j) * dk + i, fmt)"),
+    "gla_o_from_old_state": ("acc += qi * sn;", "acc += qi * sij;"),
 }
 
 
@@ -111,7 +115,24 @@ def _check_epilogue(o):
     assert y.tolist() == (2.0 * c + 0.5 * np.array([1.0, 2.0, 3.0, 4.0])).tolist()
 
 
-PINS = [_check_decode, _check_encode, _check_closed_forms, _check_bruteforce, _check_epilogue]
+def _check_gla(o):
+    def bits(x):
+        return np.asarray(x, dtype=np.float32).view(np.uint32)
+    rng = np.random.default_rng(3)
+    bh, dk, dv = 2, 3, 5
+    q = rng.integers(-3, 4, (bh, dk)).astype(np.float64)
+    k = rng.integers(-3, 4, (bh, dk)).astype(np.float64)
+    v = rng.integers(-3, 4, (bh, dv)).astype(np.float64)
+    S = rng.integers(-3, 4, (bh, dk, dv)).astype(np.float64)
+    for gk_val, decay in ((0.0, 1.0), (-np.inf, 0.0)):
+        gk = np.full((bh, dk), gk_val)
+        S_new, out, _, _ = o.gla_ref_decode(bits(q), bits(k), bits(v), bits(gk), bits(S), 0.5, "f32")
+        want = decay * S + k[:, :, None] * v[:, None, :]
+        assert (S_new == want).all()
+        assert (out == 0.5 * np.einsum("hi,hij->hj", q, want)).all()
+
+
+PINS = [_check_decode, _check_encode, _check_closed_forms, _check_bruteforce, _check_epilogue, _check_gla]
 
 
 def _failures(o):
