@@ -435,6 +435,55 @@ def run_sweep(args, dev):
     return 0
 
 
+GLA_WORKLOADS = [(2048, 128, 128, "bf16"), (2048, 128, 128, "f32"), (1024, 256, 256, "bf16"), (4096, 64, 64, "f16")]
+
+
+def run_gla(args, dev):
+    """GLA decode step (gla_decode): one JSON line per workload on stderr and
+    the list on stdout.  Each call updates one head-state buffer in place;
+    calls rotate over copies so that no call finds its state in L2."""
+    import torch
+
+    import memory_bound_gemv_02_gb300 as g
+    L = g.lib()
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    code = {"f16": g.GLA_F16, "bf16": g.GLA_BF16, "f32": g.GLA_F32}
+    s = torch.cuda.current_stream().cuda_stream
+    out = []
+    for bh, dk, dv, dt in GLA_WORKLOADS:
+        es = 4 if dt == "f32" else 2
+        state_bytes = bh * dk * dv * es
+        nbytes = 2 * state_bytes + bh * (3 * dk + 2 * dv) * es
+        copies = max(2, min(8, -(-3 * L2_BYTES // state_bytes)))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        sets = []
+        for _ in range(copies):
+            q, k, v = (torch.rand((bh, x), generator=gen, device=dev) * 2 - 1 for x in (dk, dk, dv))
+            gk = -3 * torch.rand((bh, dk), generator=gen, device=dev)
+            S = torch.randn((bh, dk, dv), generator=gen, device=dev)
+            q, k, v, gk, S = (x.to(tdt[dt]) for x in (q, k, v, gk, S))
+            o = torch.empty((bh, dv), dtype=tdt[dt], device=dev)
+            sets.append((q, k, v, gk, S, o))
+        calls = [(L.gla_decode, (q.data_ptr(), k.data_ptr(), v.data_ptr(), gk.data_ptr(), S.data_ptr(),
+                                 S.data_ptr(), o.data_ptr(), bh, dk, dv, ctypes.c_float(dk ** -0.5), code[dt], s))
+                 for q, k, v, gk, S, o in sets]
+        _, per = time_calls(L, calls, s, args.gla_steps, 10)
+        el = time_batch(calls, args.gla_steps, 10)
+        iso = statistics.median(per) * 1e3
+        b2b = el / args.gla_steps * 1e6
+        r = {"workload": f"gla_decode bh={bh} dk={dk} dv={dv} {dt} (in place)", "bytes": nbytes,
+             "us_isolated_median": round(iso, 3), "us_back_to_back": round(b2b, 3),
+             "gbs_back_to_back": round(nbytes / b2b / 1e3, 1), "gbs_isolated": round(nbytes / iso / 1e3, 1),
+             "pct_of_8tbps": round(100 * nbytes / b2b / 1e3 / NOMINAL_HBM_GBS, 1), "state_copies": copies}
+        out.append(r)
+        print(json.dumps(r), file=sys.stderr, flush=True)
+        del sets, calls
+        torch.cuda.empty_cache()
+    print(json.dumps({"gla_decode": out}), flush=True)
+    return 0
+
+
 def run_case(args, dev):
     """Run one shape a few times and exit (for profiler captures):
     --case N,K,DTYPE[,f32] [--calls C] [--config JSON]."""
@@ -471,6 +520,8 @@ def run_ours(args, world, rank, local):
         return run_sweep(args, dev)
     if args.case:
         return run_case(args, dev)
+    if args.gla:
+        return run_gla(args, dev)
 
     w = WORKLOAD
     n, k, fmt = w["n"], w["k"], w["dtype"]
@@ -618,6 +669,8 @@ def main(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--case", default=None, help="N,K,DTYPE[,f32]: run that shape --calls times, no timing")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--gla", action="store_true", help="time the GLA decode step workloads instead")
+    ap.add_argument("--gla-steps", type=int, default=300)
     ap.add_argument("--config", default=None, help="JSON launch configuration forced with --case")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -313,6 +313,28 @@ int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t str
 int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
                         int grid_split, cudaStream_t stream);
 
+/* Storage types of gla_decode(). */
+enum { GLA_F16 = 0, GLA_BF16 = 1, GLA_F32 = 2 };
+
+/*
+ * One decode step of gated linear attention (TileLang Case Studies, Case D
+ * "Background") for bh independent heads:
+ *
+ *     S_new[i][j] = exp(gk[i]) * S[i][j] + k[i] * v[j]     (i < dk, j < dv)
+ *     o[j]        = scale * sum_i q[i] * S_new[i][j]
+ *
+ * All tensors share the storage type `dtype` (GLA_F16, GLA_BF16 or GLA_F32);
+ * the arithmetic is fp32, each S_new element is rounded once when stored and
+ * o uses the unrounded values.  Layout per head h (device pointers, dense):
+ * q, k, gk at h*dk; v, o at h*dv; S, S_new at h*dk*dv, row i, column j at
+ * i*dv + j.  S_new may be S itself (in-place step) but not otherwise overlap
+ * it; o overlaps nothing.  v, o, S, S_new 16-byte aligned and dv a multiple
+ * of 8 (16-bit types) or 4 (fp32), dv / that <= 256; dk <= 4096.  dk == 0
+ * writes o = 0.  Asynchronous on `stream`; same status codes as gemv().
+ */
+int gla_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
+               void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,7 +11,7 @@ built, every call raises.
 Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_fused``, ``gemv_prepare``,
 ``gemv_plan``, ``gemv_last_config``, ``gemv_status_string``,
 ``gemv_last_cuda_error``, ``gemv_debug_inject``, ``gemv_release``,
-``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``.
+``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``, ``gla_decode``.
 """
 from __future__ import annotations
 
@@ -33,12 +33,14 @@ GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TI
 GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B, GEMV_OVERLAP_PDL_PREFETCH_BA = 0, 1, 2, 3
 GEMV_ACT_NONE, GEMV_ACT_RELU, GEMV_ACT_SIGMOID, GEMV_ACT_SILU = 0, 1, 2, 3
 GEMV_BIAS_INPUT_TYPE, GEMV_BIAS_F32 = 0, 1
+GLA_F16, GLA_BF16, GLA_F32 = 0, 1, 2
+_GLA_DTYPE = {torch.float16: GLA_F16, torch.bfloat16: GLA_BF16, torch.float32: GLA_F32}
 ACTIVATIONS = {"none": GEMV_ACT_NONE, "relu": GEMV_ACT_RELU, "sigmoid": GEMV_ACT_SIGMOID, "silu": GEMV_ACT_SILU}
 
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
 ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_fused", "gemv_prepare", "gemv_plan", "gemv_last_config",
                 "gemv_status_string", "gemv_last_cuda_error", "gemv_debug_inject",
-                "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc")
+                "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc", "gla_decode")
 
 
 class GemvConfig(ctypes.Structure):
@@ -103,6 +105,7 @@ def lib() -> ctypes.CDLL:
             L.gemv_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
             L.gemv_probe_read.argtypes = [vp, i64, vp, vp]
             L.gemv_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
+            L.gla_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, i32, vp]
             for name in ENTRY_POINTS:
                 if name != "gemv_status_string":
                     getattr(L, name).restype = i32
@@ -314,3 +317,31 @@ def gemv_splitk_noalloc(B, a, c=None, out_fp32: bool = False, grid_split: int = 
                                        _stream_handle(stream))
     _check(st, "gemv_splitk_noalloc")
     return c
+
+
+def gla_decode(q, k, v, gk, S, scale: float, S_new=None, o=None, stream=None):
+    """One gated-linear-attention decode step for bh heads: S_new =
+    diag(exp(gk)) S + outer(k, v), o = scale * q^T S_new.  Shapes: q, k, gk
+    (bh, dk); v (bh, dv); S (bh, dk, dv); one dtype (fp16, bf16 or fp32).
+    ``S_new`` may be ``S`` (in place).  Returns (S_new, o)."""
+    bh, dk, dv = S.shape
+    if q.shape != (bh, dk) or k.shape != (bh, dk) or gk.shape != (bh, dk) or v.shape != (bh, dv):
+        raise ValueError("shape mismatch")
+    dt = S.dtype
+    if dt not in _GLA_DTYPE or any(x.dtype != dt for x in (q, k, v, gk)):
+        raise TypeError("q, k, v, gk, S must share one of float16, bfloat16, float32")
+    if S_new is None:
+        S_new = torch.empty_like(S)
+    if o is None:
+        o = torch.empty((bh, dv), dtype=dt, device=S.device)
+    for x in (q, k, v, gk, S, S_new, o):
+        if not x.is_cuda or not x.is_contiguous() or x.device != S.device:
+            raise ValueError("all tensors must be contiguous CUDA tensors on one device")
+    if S_new.shape != S.shape or S_new.dtype != dt or o.shape != (bh, dv) or o.dtype != dt:
+        raise ValueError("S_new / o have the wrong shape or dtype")
+    with torch.cuda.device(S.device):
+        st = lib().gla_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), gk.data_ptr(), S.data_ptr(),
+                              S_new.data_ptr(), o.data_ptr(), bh, dk, dv, float(scale), _GLA_DTYPE[dt],
+                              _stream_handle(stream))
+    _check(st, "gla_decode")
+    return S_new, o

@@ -1,0 +1,247 @@
+// One decode step of gated linear attention on sm_103a (TileLang Case
+// Studies, Case D "Background"):
+//
+//     S_new = diag(exp(gk)) @ S + outer(k, v),    o = scale * q^T @ S_new
+//
+// per head, S of shape (dk, dv) row-major.  The step reads the state once and
+// writes it once -- bandwidth-bound like the GEMV -- and its output is a
+// transposed matrix-vector product fused into the update.
+//
+// Design: a persistent grid walks the heads.  For a head, exp(gk), k and q
+// are staged in shared memory (fp32); thread t owns the 16-byte column chunk
+// t % (dv / VEC) of rows t / (dv / VEC), t / (dv / VEC) + RP, ... (so a warp's
+// loads and stores cover contiguous rows: fully coalesced), updates each
+// element as fmaf(exp(gk_i), S_ij, k_i v_j) in fp32, stores it rounded once,
+// and accumulates q_i * S_new_ij (unrounded) for its columns.  The RP row
+// partials of each column are added in shared memory in row-block order, so
+// the result is deterministic.  Four rows are in flight per thread.
+// S_new may be S itself (an in-place step): every element is read and then
+// written by the same thread.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemv.h"
+#include "gemv_kernels.cuh"
+
+namespace gemvk {
+namespace {
+
+struct GlaParams {
+  const void *q, *k, *v, *gk, *S;
+  void *S_new, *o;
+  int64_t bh;
+  int32_t dk, dv;
+  float scale;
+};
+
+struct F32 {};  // tag of the fp32 storage type
+
+// Element access for the three storage types: VEC elements per 16 bytes.
+template <class T>
+struct GlaIo;
+
+template <>
+struct GlaIo<F16> {
+  static constexpr int VEC = 8;
+  static __device__ __forceinline__ float scalar(const void *p, int64_t i) {
+    return F16::to_float(static_cast<const uint16_t *>(p)[i]);
+  }
+  static __device__ __forceinline__ void unpack(const uint4 &w, float (&f)[VEC]) { widen8<F16>(w, f); }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[VEC]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = (uint32_t)F16::from_float(f[2 * q]) | ((uint32_t)F16::from_float(f[2 * q + 1]) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
+    static_cast<uint16_t *>(p)[i] = F16::from_float(x);
+  }
+};
+
+template <>
+struct GlaIo<BF16> {
+  static constexpr int VEC = 8;
+  static __device__ __forceinline__ float scalar(const void *p, int64_t i) {
+    return BF16::to_float(static_cast<const uint16_t *>(p)[i]);
+  }
+  static __device__ __forceinline__ void unpack(const uint4 &w, float (&f)[VEC]) { widen8<BF16>(w, f); }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[VEC]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = (uint32_t)BF16::from_float(f[2 * q]) | ((uint32_t)BF16::from_float(f[2 * q + 1]) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
+    static_cast<uint16_t *>(p)[i] = BF16::from_float(x);
+  }
+};
+
+template <>
+struct GlaIo<F32> {
+  static constexpr int VEC = 4;
+  static __device__ __forceinline__ float scalar(const void *p, int64_t i) {
+    return static_cast<const float *>(p)[i];
+  }
+  static __device__ __forceinline__ void unpack(const uint4 &w, float (&f)[VEC]) {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y); f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[VEC]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+  static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
+    static_cast<float *>(p)[i] = x;
+  }
+};
+
+constexpr int kGlaThreads = 256;
+constexpr int kGlaMaxDk = 4096;
+constexpr int kGlaRowsInFlight = 4;
+
+// 16-byte store of data written once (no L1 allocation needed).
+__device__ __forceinline__ void stg_stream(uint4 *p, const uint4 &v) {
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+template <class T>
+__global__ void __launch_bounds__(kGlaThreads) gla_decode_kernel(GlaParams p) {
+  using IO = GlaIo<T>;
+  constexpr int VEC = IO::VEC;
+  extern __shared__ float gsm[];
+  const int dk = p.dk, dv = p.dv;
+  float *dec = gsm;           // exp(gk)   [dk]
+  float *kk = dec + dk;       // k         [dk]
+  float *qq = kk + dk;        // q         [dk]
+  float *part = qq + dk;      // row-block partials of o [RP][dv]
+  const int cpr = dv / VEC;   // 16-byte chunks per row
+  const int RP = kGlaThreads / cpr;  // row blocks (>= 1: the host keeps cpr <= kGlaThreads)
+  const int t = threadIdx.x;
+  const int cc = t % cpr, rl = t / cpr;
+  const bool active = rl < RP;
+
+  for (int64_t h = blockIdx.x; h < p.bh; h += gridDim.x) {
+    for (int i = t; i < dk; i += kGlaThreads) {
+      dec[i] = expf(IO::scalar(p.gk, h * dk + i));
+      kk[i] = IO::scalar(p.k, h * dk + i);
+      qq[i] = IO::scalar(p.q, h * dk + i);
+    }
+    __syncthreads();
+    if (active) {
+      // this thread's VEC elements of v (16-byte aligned: dv % VEC == 0)
+      float vv[VEC];
+      IO::unpack(__ldg(reinterpret_cast<const uint4 *>(p.v) + (h * dv) / VEC + cc), vv);
+      float acc[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+      const uint4 *Srow = reinterpret_cast<const uint4 *>(p.S) + (h * dk) * (int64_t)cpr + cc;
+      uint4 *Nrow = reinterpret_cast<uint4 *>(p.S_new) + (h * dk) * (int64_t)cpr + cc;
+      for (int i0 = rl; i0 < dk; i0 += RP * kGlaRowsInFlight) {
+        uint4 sv[kGlaRowsInFlight];
+#pragma unroll
+        for (int u = 0; u < kGlaRowsInFlight; ++u) {
+          const int i = i0 + u * RP;
+          sv[u] = (i < dk) ? ldg_stream(Srow + (int64_t)i * cpr) : zero4();
+        }
+#pragma unroll
+        for (int u = 0; u < kGlaRowsInFlight; ++u) {
+          const int i = i0 + u * RP;
+          if (i < dk) {
+            float s[VEC], sn[VEC];
+            IO::unpack(sv[u], s);
+            const float di = dec[i], ki = kk[i], qi = qq[i];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              sn[e] = fmaf(di, s[e], ki * vv[e]);
+              acc[e] = fmaf(qi, sn[e], acc[e]);
+            }
+            stg_stream(Nrow + (int64_t)i * cpr, IO::pack(sn));
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) part[rl * dv + cc * VEC + e] = acc[e];
+    }
+    __syncthreads();
+    for (int j = t; j < dv; j += kGlaThreads) {
+      float sum = 0.f;
+      for (int r = 0; r < RP; ++r) sum += part[r * dv + j];
+      IO::store_scalar(p.o, h * dv + j, p.scale * sum);
+    }
+    __syncthreads();  // dec/kk/qq/part are reused by the next head
+  }
+}
+
+bool overlap_bytes(const void *p, int64_t pb, const void *q, int64_t qb) {
+  const uintptr_t a0 = (uintptr_t)p, a1 = a0 + (uintptr_t)pb;
+  const uintptr_t b0 = (uintptr_t)q, b1 = b0 + (uintptr_t)qb;
+  return a0 < b1 && b0 < a1;
+}
+
+}  // namespace
+}  // namespace gemvk
+
+using namespace gemvk;
+
+extern "C" int gla_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
+                          void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, cudaStream_t stream) {
+  if (dtype != GLA_F16 && dtype != GLA_BF16 && dtype != GLA_F32) return GEMV_ERR_DTYPE;
+  if (bh < 0 || dk < 0 || dv < 0 || dk > kGlaMaxDk) return GEMV_ERR_ARG;
+  if (bh == 0 || dv == 0) return GEMV_OK;
+  const int es = dtype == GLA_F32 ? 4 : 2;
+  const int VEC = 16 / es;
+  if (dv % VEC != 0 || dv / VEC > kGlaThreads) return GEMV_ERR_ARG;
+  if (o == nullptr || v == nullptr) return GEMV_ERR_ARG;
+  if (dk > 0 && (q == nullptr || k == nullptr || gk == nullptr || S == nullptr || S_new == nullptr))
+    return GEMV_ERR_ARG;
+  if (((uintptr_t)v | (uintptr_t)o) & 15u) return GEMV_ERR_ALIGN;
+  if (dk > 0 && (((uintptr_t)S | (uintptr_t)S_new) & 15u)) return GEMV_ERR_ALIGN;
+  if (dk > 0 && (((uintptr_t)q | (uintptr_t)k | (uintptr_t)gk) % (uintptr_t)es)) return GEMV_ERR_ALIGN;
+  const int64_t sbytes = bh * dk * dv * es, obytes = bh * dv * es, vecbytes = bh * dk * es;
+  // S_new may be S itself (in place), but must not partly overlap it; o
+  // overlaps nothing.
+  if (dk > 0 && S_new != S && overlap_bytes(S_new, sbytes, S, sbytes)) return GEMV_ERR_ALIAS;
+  if (overlap_bytes(o, obytes, v, obytes)) return GEMV_ERR_ALIAS;
+  if (dk > 0 && (overlap_bytes(o, obytes, S, sbytes) || overlap_bytes(o, obytes, S_new, sbytes) ||
+                 overlap_bytes(o, obytes, q, vecbytes) || overlap_bytes(o, obytes, k, vecbytes) ||
+                 overlap_bytes(o, obytes, gk, vecbytes)))
+    return GEMV_ERR_ALIAS;
+  if (dk > 0 && (overlap_bytes(S_new, sbytes, q, vecbytes) || overlap_bytes(S_new, sbytes, k, vecbytes) ||
+                 overlap_bytes(S_new, sbytes, gk, vecbytes) || overlap_bytes(S_new, sbytes, v, obytes)))
+    return GEMV_ERR_ALIAS;
+
+  int dev = -1, sms = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  if (major != 10 || minor != 3) return GEMV_ERR_DEVICE;
+  const int cpr = (int)(dv / VEC);
+  const int RP = kGlaThreads / cpr;
+  const size_t smem = (size_t)(3 * dk + (int64_t)RP * dv) * sizeof(float);
+  GlaParams p;
+  p.q = q; p.k = k; p.v = v; p.gk = gk; p.S = S; p.S_new = S_new; p.o = o;
+  p.bh = bh; p.dk = (int32_t)dk; p.dv = (int32_t)dv; p.scale = scale;
+  void (*fn)(GlaParams) = dtype == GLA_F16 ? gla_decode_kernel<F16>
+                          : dtype == GLA_BF16 ? gla_decode_kernel<BF16> : gla_decode_kernel<F32>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute((const void *)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return GEMV_ERR_CUDA;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, kGlaThreads, smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    return GEMV_ERR_CONFIG;
+  }
+  int64_t grid = (int64_t)sms * per_sm;
+  if (grid > bh) grid = bh;
+  fn<<<(unsigned)grid, kGlaThreads, smem, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return GEMV_ERR_CUDA;
+  return GEMV_OK;
+}

@@ -211,3 +211,33 @@ def staged_shifted(a, j0, seglen, off, as_elems):
         pair = np.concatenate([src(q - 1), src(q)])
         out[8 * q: 8 * q + 8] = pair[sh: sh + 8]
     return out
+
+
+
+def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=4):
+    """Index replay of ``gla_decode_kernel``: every state element of every head
+    is read and written exactly once by one thread, every partial slot and
+    every output element is in range."""
+    vec = 16 // elem_bytes
+    assert dv % vec == 0
+    cpr = dv // vec
+    assert 1 <= cpr <= threads
+    RP = threads // cpr
+    touched = np.zeros((bh, dk, dv), dtype=np.int32)
+    smem_floats = 3 * dk + RP * dv
+    for h in range(bh):
+        for t in range(threads):
+            cc, rl = t % cpr, t // cpr
+            if rl >= RP:
+                continue
+            for i0 in range(rl, dk, RP * rows_in_flight):
+                for u in range(rows_in_flight):
+                    i = i0 + u * RP
+                    if i < dk:
+                        vidx = (h * dk + i) * cpr + cc  # 16-byte vector index of S / S_new
+                        assert 0 <= vidx < bh * dk * cpr
+                        touched[h, i, cc * vec:(cc + 1) * vec] += 1
+            assert 3 * dk + rl * dv + cc * vec + vec <= smem_floats
+            assert (h * dv) // vec + cc < bh * dv // vec
+    assert (touched == 1).all()
+    return {"smem_floats": smem_floats}

@@ -1,0 +1,142 @@
+"""GLA decode step on the GPU (gla_decode) against the oracle.
+
+S_new = diag(exp(gk)) S + outer(k, v), o = scale * q^T S_new per head
+(TileLang Case Studies, Case D "Background").  The kernel works in fp32 and
+rounds each stored value once; the oracle works in binary64.
+
+Tolerances, from the arithmetic: an S_new element is fmaf(exp(gk), S,
+k*v) -- a few fp32 roundings plus expf's error, within 8 u32 of
+|exp(gk) S| + |k v| -- then rounded once to the storage type (half an ulp).
+o sums dk fp32 products: within 1e-5 * |scale| sum |q S_new| plus the S_new
+errors it carries (|scale| sum |q| 8 u32 (|exp(gk) S| + |k v|)), then rounded
+to the storage type.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_gemv_02_gb300 as g
+import oracle
+import parity_rules
+
+pytestmark = pytest.mark.gpu
+
+U32 = 2.0 ** -24
+FMT = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
+
+
+def _bits(t):
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy().view(np.uint32)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _make(bh, dk, dv, dtype, seed, dev):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+
+    def u(*shape, lo=-1.0, hi=1.0):
+        return (torch.rand(shape, generator=gen, device=dev) * (hi - lo) + lo).to(dtype)
+    q, k, v = u(bh, dk), u(bh, dk), u(bh, dv)
+    gk = u(bh, dk, lo=-3.0, hi=0.0)
+    S = (torch.randn((bh, dk, dv), generator=gen, device=dev)).to(dtype)
+    return q, k, v, gk, S
+
+
+def _check(q, k, v, gk, S_in, S_new, o, scale, label):
+    torch.cuda.synchronize()
+    fmt = FMT[S_in.dtype]
+    ref_S, ref_o, ss, os_ = oracle.gla_ref_decode(_bits(q), _bits(k), _bits(v), _bits(gk), _bits(S_in), scale, fmt)
+    got_S = S_new.double().cpu().numpy()
+    got_o = o.double().cpu().numpy()
+    tol_S = 8 * U32 * ss + (0 if fmt == "f32" else 0.5) * parity_rules.ulp(ref_S, fmt)
+    # o inherits the fp32 error of each S_new element it sums (which is
+    # relative to |exp(gk) S| + |k v|, not to |S_new|) plus its own sum's.
+    qd = q.double().cpu().numpy()
+    carried = abs(scale) * np.einsum("hi,hij->hj", np.abs(qd), 8 * U32 * ss)
+    tol_o = 1e-5 * os_ + carried + (0 if fmt == "f32" else 0.5) * parity_rules.ulp(ref_o, fmt) + 1e-30
+    bad_S = ~(np.abs(got_S - ref_S) <= tol_S)
+    bad_o = ~(np.abs(got_o - ref_o) <= tol_o)
+    assert not bad_S.any(), f"{label}: S_new off at {np.argwhere(bad_S)[:4].tolist()}"
+    assert not bad_o.any(), f"{label}: o off at {np.argwhere(bad_o)[:4].tolist()}"
+    for err, ref in ((got_S - ref_S, ref_S), (got_o - ref_o, ref_o)):
+        assert not parity_rules.pow2_errors(err, ref, fmt).any(), f"{label}: power-of-two error pattern"
+
+
+SHAPES = [(64, 128, 128), (32, 64, 64), (8, 256, 128), (3, 17, 8), (2, 1, 512), (4, 100, 1024), (1, 4096, 64)]
+
+
+@pytest.mark.parametrize("bh,dk,dv", SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_gla_parity(cuda_dev, bh, dk, dv, dtype):
+    if dtype == torch.float32 and dv // 4 > 256:
+        pytest.skip("dv / 4 > 256 is outside the kernel's range for fp32")
+    q, k, v, gk, S = _make(bh, dk, dv, dtype, bh + dk + dv, cuda_dev)
+    S_in = S.clone()
+    S_new, o = g.gla_decode(q, k, v, gk, S, scale=dk ** -0.5)
+    _check(q, k, v, gk, S_in, S_new, o, dk ** -0.5, f"{bh}x{dk}x{dv} {dtype}")
+    assert torch.equal(S, S_in)  # out of place: S untouched
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_gla_in_place(cuda_dev, dtype):
+    q, k, v, gk, S = _make(16, 128, 128, dtype, 5, cuda_dev)
+    S_in = S.clone()
+    S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.125, S_new=S)
+    assert S_new.data_ptr() == S.data_ptr()
+    _check(q, k, v, gk, S_in, S_new, o, 0.125, f"in place {dtype}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype):
+    """gk = 0 and small integers: every fp32 operation is exact, so the stored
+    state and o equal the oracle rounded once."""
+    gen = torch.Generator(device=cuda_dev)
+    gen.manual_seed(3)
+    bh, dk, dv = 8, 64, 128
+    ri = lambda *s: torch.randint(-3, 4, s, generator=gen, device=cuda_dev).to(dtype)
+    q, k, v, S = ri(bh, dk), ri(bh, dk), ri(bh, dv), ri(bh, dk, dv)
+    gk = torch.zeros((bh, dk), dtype=dtype, device=cuda_dev)
+    S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.5)
+    torch.cuda.synchronize()
+    fmt = FMT[dtype]
+    ref_S, ref_o, _, _ = oracle.gla_ref_decode(_bits(q), _bits(k), _bits(v), _bits(gk), _bits(S), 0.5, fmt)
+    assert (_bits(S_new) == oracle.encode(ref_S, fmt)).all()
+    assert (_bits(o) == oracle.encode(ref_o, fmt)).all()
+
+
+def test_gla_multiple_steps_match_stepwise_oracle(cuda_dev):
+    """Ten chained decode steps on one state (in place), each checked."""
+    bh, dk, dv = 12, 64, 64
+    q, k, v, gk, S = _make(bh, dk, dv, torch.float32, 9, cuda_dev)
+    for step in range(10):
+        q, k, v, gk, _ = _make(bh, dk, dv, torch.float32, 100 + step, cuda_dev)
+        S_prev = S.clone()
+        _, o = g.gla_decode(q, k, v, gk, S, scale=0.1, S_new=S)
+        _check(q, k, v, gk, S_prev, S, o, 0.1, f"step {step}")
+
+
+def test_gla_empty_dk_and_errors(cuda_dev):
+    bh, dv = 3, 64
+    z = torch.empty((bh, 0), dtype=torch.bfloat16, device=cuda_dev)
+    S = torch.empty((bh, 0, dv), dtype=torch.bfloat16, device=cuda_dev)
+    v = torch.ones((bh, dv), dtype=torch.bfloat16, device=cuda_dev)
+    o = torch.full((bh, dv), 7.0, dtype=torch.bfloat16, device=cuda_dev)
+    g.gla_decode(z, z, v, z, S, scale=1.0, o=o)
+    torch.cuda.synchronize()
+    assert (o == 0).all()
+    q, k, v, gk, S = _make(2, 16, 24, torch.bfloat16, 1, cuda_dev)
+    with pytest.raises(g.GemvError) as ei:
+        g.gla_decode(q, k, v, gk, S, scale=1.0)  # dv = 24 is a multiple of 8: fine
+        g.gla_decode(q, k, v[:, :20].contiguous(), gk, S[:, :, :20].contiguous(), scale=1.0)  # 20 % 8 != 0
+    assert ei.value.status == g.GEMV_ERR_ARG
+    base = torch.zeros(2 * 16 * 32 + 8, dtype=torch.bfloat16, device=cuda_dev)
+    S0 = base[:2 * 16 * 32].view(2, 16, 32)
+    S1 = base[8:8 + 2 * 16 * 32].view(2, 16, 32)  # 16 bytes further: overlaps S0, is not S0
+    with pytest.raises(g.GemvError) as ei:
+        g.gla_decode(q, k, torch.zeros((2, 32), dtype=torch.bfloat16, device=cuda_dev), gk, S0, scale=1.0,
+                     S_new=S1)
+    assert ei.value.status == g.GEMV_ERR_ALIAS

@@ -199,3 +199,9 @@ def test_tiles_index_replay_strided(gemv_lib, n, k, ldb, base_off, forced):
     except gemv_lib.GemvError:
         pytest.skip("configuration not valid for this shape")
     kernel_model.replay(n, k, cfg, base_off=base_off, ldb=ldb)
+
+
+@pytest.mark.parametrize("bh,dk,dv,es", [(3, 128, 128, 2), (2, 64, 64, 4), (5, 17, 8, 2), (1, 1, 2048, 2),
+                                         (2, 100, 1024, 4), (4, 256, 24, 2), (1, 0, 64, 2)])
+def test_gla_index_replay(bh, dk, dv, es):
+    kernel_model.replay_gla(bh, dk, dv, es)
