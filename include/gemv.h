@@ -66,10 +66,19 @@ enum {
   GEMV_VARIANT_ROWS_GENERAL = 2, /* any k and any 2-byte-aligned B: each row is read as the
                                     aligned 16-byte blocks covering it, edge elements masked,
                                     and a is realigned in registers by the row's offset */
-  GEMV_VARIANT_TILES = 3         /* any alignment: CTAs take interleaved tiles of rows of one
+  GEMV_VARIANT_TILES = 3,        /* any alignment: CTAs take interleaved tiles of rows of one
                                     residue class (row index mod 8, so one block offset per
                                     CTA), a is staged pre-shifted, rows are split into
                                     warp_split slices combined in shared memory */
+  GEMV_VARIANT_BULK = 4          /* the tiles variant's work split (one row per warp), with B
+                                    staged in shared memory instead of registers: each warp
+                                    keeps a ring of `stages` buffers of 32*unroll 16-byte
+                                    blocks that 1-D bulk asynchronous copies (TMA,
+                                    cp.async.bulk, no multicast) fill from global memory,
+                                    completion tracked by one mbarrier per buffer.  The
+                                    sm_103a form of the multi-stage shared-memory pipeline of
+                                    B (TileLang Case Studies, Case B.1 "O3 Pipelined B
+                                    Loads"); chosen only when forced */
 };
 
 /* Launch overlap with the preceding work on the stream (gemv_config.overlap). */
@@ -124,6 +133,9 @@ enum {
  *                 L2 to prefetch its slice of the tile this many rounds
  *                 ahead (one bulk prefetch per row slice; 0 = none, at most
  *                 3; -1 forces 0 when forcing).
+ *  stages         bulk variant: buffers in each warp's ring (2 .. 8; the
+ *                 planner takes the most of 4, 3, 2 that fit in shared
+ *                 memory).  0 for the other variants.
  */
 typedef struct gemv_config {
   int32_t variant;
@@ -139,7 +151,8 @@ typedef struct gemv_config {
   int32_t unroll;
   int32_t overlap;
   int32_t l2_prefetch;
-  int32_t reserved[2];
+  int32_t stages;
+  int32_t reserved;
 } gemv_config;
 
 /*
@@ -253,6 +266,25 @@ int gemv_last_cuda_error(void);
  * GPU fault is ever involved.
  */
 int gemv_debug_inject(int status);
+
+/*
+ * Waits of the bulk variant that gave up.  Each wait of a warp on one of its
+ * ring buffers polls the buffer's mbarrier a bounded number of times (2^20);
+ * a warp whose wait runs out stops issuing copies, waits (again bounded) for
+ * the copies it already issued, writes NaN for the rows it owns and adds one
+ * to a per-device counter.  This reads that counter for the current device
+ * into *count (synchronously: it waits for the device's outstanding work),
+ * then zeroes it if `reset` is nonzero.
+ */
+int gemv_wait_timeouts(int reset, uint32_t *count);
+
+/*
+ * Test hook: the next launch of the bulk variant (on any thread) gives each
+ * ring wait `polls` polls instead of 2^20 (0 = every wait gives up at once,
+ * exercising the path above without any hang); -1 clears it.  The waits
+ * that drain copies already issued keep the full limit.
+ */
+int gemv_debug_wait_budget(int32_t polls);
 
 /*
  * Free the library-owned workspaces and drop the configuration cache.  The

@@ -11,7 +11,8 @@ built, every call raises.
 Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_fused``, ``gemv_prepare``,
 ``gemv_plan``, ``gemv_last_config``, ``gemv_status_string``,
 ``gemv_last_cuda_error``, ``gemv_debug_inject``, ``gemv_release``,
-``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``, ``gla_decode``.
+``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``, ``gemv_wait_timeouts``,
+``gemv_debug_wait_budget``, ``gla_decode``.
 """
 from __future__ import annotations
 
@@ -30,6 +31,7 @@ GEMV_ERR_CUDA, GEMV_ERR_CONFIG, GEMV_ERR_ALIGN, GEMV_ERR_NOMEM = -5, -6, -7, -8
 GEMV_ERR_SCRATCH = -9
 GEMV_STATIC_SCRATCH_FLOATS = 1 << 20
 GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TILES = 0, 1, 2, 3
+GEMV_VARIANT_BULK = 4
 GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B, GEMV_OVERLAP_PDL_PREFETCH_BA = 0, 1, 2, 3
 GEMV_ACT_NONE, GEMV_ACT_RELU, GEMV_ACT_SIGMOID, GEMV_ACT_SILU = 0, 1, 2, 3
 GEMV_BIAS_INPUT_TYPE, GEMV_BIAS_F32 = 0, 1
@@ -40,7 +42,8 @@ ACTIVATIONS = {"none": GEMV_ACT_NONE, "relu": GEMV_ACT_RELU, "sigmoid": GEMV_ACT
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
 ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_fused", "gemv_prepare", "gemv_plan", "gemv_last_config",
                 "gemv_status_string", "gemv_last_cuda_error", "gemv_debug_inject",
-                "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc", "gla_decode")
+                "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc",
+                "gemv_wait_timeouts", "gemv_debug_wait_budget", "gla_decode")
 
 
 class GemvConfig(ctypes.Structure):
@@ -51,7 +54,7 @@ class GemvConfig(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("k_segment", ctypes.c_int64), ("row_blocks", ctypes.c_int32),
                 ("unroll", ctypes.c_int32), ("overlap", ctypes.c_int32),
-                ("l2_prefetch", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+                ("l2_prefetch", ctypes.c_int32), ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def to_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
@@ -105,6 +108,8 @@ def lib() -> ctypes.CDLL:
             L.gemv_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
             L.gemv_probe_read.argtypes = [vp, i64, vp, vp]
             L.gemv_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
+            L.gemv_wait_timeouts.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32)]
+            L.gemv_debug_wait_budget.argtypes = [ctypes.c_int32]
             L.gla_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, i32, vp]
             for name in ENTRY_POINTS:
                 if name != "gemv_status_string":
@@ -317,6 +322,20 @@ def gemv_splitk_noalloc(B, a, c=None, out_fp32: bool = False, grid_split: int = 
                                        _stream_handle(stream))
     _check(st, "gemv_splitk_noalloc")
     return c
+
+
+def gemv_wait_timeouts(reset: bool = False) -> int:
+    """Ring waits of the bulk variant that gave up on the current device
+    (synchronizes the device); ``reset`` zeroes the counter after reading."""
+    out = ctypes.c_uint32(0)
+    _check(lib().gemv_wait_timeouts(1 if reset else 0, ctypes.byref(out)), "gemv_wait_timeouts")
+    return int(out.value)
+
+
+def gemv_debug_wait_budget(polls: int) -> None:
+    """Test hook: the next bulk-variant launch polls each ring wait at most
+    ``polls`` times (0: every wait gives up at once); -1 clears it."""
+    _check(lib().gemv_debug_wait_budget(int(polls)), "gemv_debug_wait_budget")
 
 
 def gla_decode(q, k, v, gk, S, scale: float, S_new=None, o=None, stream=None):

@@ -21,8 +21,10 @@ OBJDIR = os.path.join(ROOT, "_build", "gemv")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgemv.so")
 
-SOURCES = ["gemv_api.cu", "gemv_kernels_f16.cu", "gemv_kernels_bf16.cu", "gemv_probe.cu", "gla_decode.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("gemv_internal.h", "gemv_kernels.cuh", "gemv_tiles.cuh")] + \
+SOURCES = ["gemv_api.cu", "gemv_kernels_f16.cu", "gemv_kernels_bf16.cu", "gemv_bulk_f16.cu", "gemv_bulk_bf16.cu",
+           "gemv_probe.cu", "gla_decode.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("gemv_internal.h", "gemv_kernels.cuh", "gemv_tiles.cuh",
+                                           "gemv_bulk.cuh")] + \
     [os.path.join(INCLUDE, "gemv.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

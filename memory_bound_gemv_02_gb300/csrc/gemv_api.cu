@@ -22,6 +22,10 @@
 #include "gemv.h"
 #include "gemv_internal.h"
 
+// Ring waits of the bulk kernel that gave up, on each device that loads this
+// library (read and cleared by gemv_wait_timeouts()).
+static __device__ uint32_t g_gemv_wait_timeouts;
+
 namespace gemvk {
 namespace {
 
@@ -90,6 +94,9 @@ std::unordered_map<Key, gemv_config, KeyHash> g_cache;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 std::set<std::pair<const void *, int>> g_func_attr_set;
 std::atomic<int> g_inject{0};
+std::atomic<int> g_wait_budget{-1};  // one-shot poll budget of the next bulk launch (-1: none)
+
+uint32_t *g_timeouts_ptr[kMaxDevices] = {};  // device address of g_gemv_wait_timeouts, per device (g_mu)
 
 thread_local gemv_config t_last{};
 thread_local bool t_has_last = false;
@@ -131,7 +138,8 @@ bool valid_tiles_RU(int R, int U) {
 //    at most 8 loads per lane; short rows are instead streamed R at a time.
 //  * C (CTAs per segment): every SM busy at 32 resident warps, a multiple
 //    of 8 (one row class per CTA) unless the rows are 16-byte aligned.
-int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f, gemv_config *out) {
+int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f, gemv_config *out,
+               bool bulk = false) {
   const int NCLS = aligned ? 1 : 8;
   const int W_list[3] = {16, 8, 4};
   gemv_config best{};
@@ -170,7 +178,13 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
       }
     }
     int R, U;
-    if (f->rows_per_warp || f->unroll) {
+    if (bulk) {
+      // One row per warp; a ring buffer is 32 * U blocks.
+      if (f->rows_per_warp > 1) return GEMV_ERR_CONFIG;
+      R = 1;
+      U = f->unroll ? f->unroll : (cdiv(nt_est, S) <= 128 ? 4 : 8);
+      if (U != 4 && U != 8) return GEMV_ERR_CONFIG;
+    } else if (f->rows_per_warp || f->unroll) {
       R = f->rows_per_warp ? f->rows_per_warp : 1;
       U = f->unroll ? f->unroll : (R == 1 ? 8 : (R == 2 ? 4 : 2));
       if (!valid_tiles_RU(R, U)) return GEMV_ERR_CONFIG;
@@ -191,7 +205,19 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     const int64_t rows_per_class = cdiv(n, NCLS);
     const int64_t groups = cdiv(rows_per_class, RT);  // tiles per class per segment
     const int64_t as_elems = round_up(kseg + 24, 8);
-    const int64_t smem = as_elems * 2 + 2LL * W * R * 4;
+    int NS = 0;  // bulk: ring buffers per warp
+    if (bulk) {
+      if (f->stages) {
+        NS = f->stages;
+        if (NS < 2 || NS > 8) return GEMV_ERR_CONFIG;
+      } else {
+        for (NS = 4; NS > 2 && bulk_smem_bytes(as_elems, W, U, NS) > kMaxSmemPerCta; --NS) {
+        }
+      }
+    } else if (f->stages) {
+      return GEMV_ERR_CONFIG;
+    }
+    const int64_t smem = bulk ? bulk_smem_bytes(as_elems, W, U, NS) : as_elems * 2 + 2LL * W * R * 4;
     if (smem > kMaxSmemPerCta) return GEMV_ERR_CONFIG;
     int cps = cps_warps;
     const int64_t cps_smem = kSmemPerSm / (smem + kSmemReservedPerCta);
@@ -223,7 +249,7 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     if (C * Sg > INT32_MAX) return GEMV_ERR_CONFIG;
 
     gemv_config c{};
-    c.variant = GEMV_VARIANT_TILES;
+    c.variant = bulk ? GEMV_VARIANT_BULK : GEMV_VARIANT_TILES;
     c.rows_per_warp = R;
     c.unroll = U;
     c.warps_per_cta = W;
@@ -231,11 +257,17 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     c.grid_split = (int32_t)Sg;
     c.row_blocks = (int32_t)C;
     c.ctas = (int32_t)(C * Sg);
-    c.smem_bytes = (int32_t)(round_up(kseg + 24, 8) * 2 + 2LL * W * R * 4);
+    if (bulk && !f->stages) {
+      // A shorter final segment may leave room for a deeper ring.
+      while (NS < 4 && bulk_smem_bytes(round_up(kseg + 24, 8), W, U, NS + 1) <= kMaxSmemPerCta) ++NS;
+    }
+    c.smem_bytes = (int32_t)(bulk ? bulk_smem_bytes(round_up(kseg + 24, 8), W, U, NS)
+                                  : round_up(kseg + 24, 8) * 2 + 2LL * W * R * 4);
+    c.stages = NS;
     c.launches = Sg > 1 ? 2 : 1;
     c.k_segment = kseg;
     if (f->l2_prefetch) {
-      if (f->l2_prefetch < -1 || f->l2_prefetch > 3) return GEMV_ERR_CONFIG;
+      if (f->l2_prefetch < -1 || f->l2_prefetch > 3 || (bulk && f->l2_prefetch > 0)) return GEMV_ERR_CONFIG;
       c.l2_prefetch = f->l2_prefetch < 0 ? 0 : f->l2_prefetch;
     } else {
       c.l2_prefetch = kDefaultL2Prefetch;
@@ -261,6 +293,8 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
                                                                             : kAutoVariant;
   const int variant = f->variant ? f->variant : auto_variant;
   if (variant == GEMV_VARIANT_TILES) return plan_tiles(n, k, aligned, sm, f, out);
+  if (variant == GEMV_VARIANT_BULK) return plan_tiles(n, k, aligned, sm, f, out, true);
+  if (f->stages) return GEMV_ERR_CONFIG;
   if (variant != GEMV_VARIANT_ROWS && variant != GEMV_VARIANT_ROWS_GENERAL) return GEMV_ERR_CONFIG;
   if (variant == GEMV_VARIANT_ROWS && !aligned) return GEMV_ERR_CONFIG;
 
@@ -365,6 +399,10 @@ MainKernel lookup_main(int dtype, const gemv_config &c, bool aligned, bool epi =
     return (dtype & 1) ? tiles_kernel_bf16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll, epi ? 1 : 0)
                        : tiles_kernel_f16(of, aligned ? 1 : 0, c.rows_per_warp, c.unroll, epi ? 1 : 0);
   }
+  if (c.variant == GEMV_VARIANT_BULK) {
+    return (dtype & 1) ? bulk_kernel_bf16(of, aligned ? 1 : 0, c.unroll, epi ? 1 : 0)
+                       : bulk_kernel_f16(of, aligned ? 1 : 0, c.unroll, epi ? 1 : 0);
+  }
   return (dtype & 1) ? main_kernel_bf16(of, c.variant, c.rows_per_warp)
                      : main_kernel_f16(of, c.variant, c.rows_per_warp);
 }
@@ -454,6 +492,23 @@ bool is_identity(const Epilogue &ep) {
   return ep.alpha == 1.f && ep.bias == nullptr && ep.act == GEMV_ACT_NONE;
 }
 
+// Device address of the timeout counter on `dev` (the current device),
+// looked up once per device.
+int timeout_counter(int dev, uint32_t **out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_timeouts_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_gemv_wait_timeouts);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    }
+    g_timeouts_ptr[dev] = static_cast<uint32_t *>(p);
+  }
+  *out = g_timeouts_ptr[dev];
+  return GEMV_OK;
+}
+
 int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_t k, int dtype,
            const gemv_config *forced, const Epilogue &ep, cudaStream_t stream) {
   int inj = g_inject.exchange(0);
@@ -500,7 +555,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
     const bool is_forced = forced != nullptr && (forced->variant || forced->rows_per_warp ||
                                                  forced->warps_per_cta || forced->warp_split ||
                                                  forced->grid_split || forced->ctas || forced->unroll ||
-                                                 forced->l2_prefetch);
+                                                 forced->l2_prefetch || forced->stages);
     if (is_forced) {
       st = plan_impl(n, k, dtype, aligned, di.sm_count, forced, &cfg);
       if (st != GEMV_OK) return st;
@@ -541,6 +596,15 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   p.nrb = cfg.row_blocks;
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
   p.ep = ep;
+  p.stages = cfg.stages;
+  p.wait_polls = kWaitPolls;
+  p.timeouts = nullptr;
+  if (cfg.variant == GEMV_VARIANT_BULK) {
+    st = timeout_counter(dev, &p.timeouts);
+    if (st != GEMV_OK) return st;
+    const int budget = g_wait_budget.exchange(-1);
+    if (budget >= 0) p.wait_polls = budget;
+  }
   p.flags = ((overlap >= GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
             ((overlap == GEMV_OVERLAP_PDL_PREFETCH_BA) ? kFlagPrefetchA : 0) |
             (is_identity(ep) ? 0 : kFlagEpilogue) | (cfg.l2_prefetch << kFlagL2Shift);
@@ -682,6 +746,33 @@ extern "C" int gemv_last_cuda_error(void) { return t_cuda_err; }
 
 extern "C" int gemv_debug_inject(int status) {
   g_inject.store(status);
+  return GEMV_OK;
+}
+
+extern "C" int gemv_debug_wait_budget(int32_t polls) {
+  if (polls < -1) return GEMV_ERR_ARG;
+  g_wait_budget.store(polls);
+  return GEMV_OK;
+}
+
+extern "C" int gemv_wait_timeouts(int reset, uint32_t *count) {
+  if (count == nullptr) return GEMV_ERR_ARG;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  uint32_t *ptr = nullptr;
+  int st = timeout_counter(dev, &ptr);
+  if (st != GEMV_OK) return st;
+  e = cudaMemcpy(count, ptr, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (reset) {
+    e = cudaMemset(ptr, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return GEMV_OK;
 }
 
@@ -848,6 +939,9 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
   p.as_elems = (int32_t)round_up(cfg.k_segment + 24, 8);
   p.flags = 0;
   p.ep = identity_epilogue();
+  p.stages = 0;
+  p.wait_polls = kWaitPolls;
+  p.timeouts = nullptr;
   // Every (segment, row) partial is written by the first kernel before the
   // second reads it, so the scratch needs no clearing between calls.
   mk<<<cfg.ctas, cfg.warps_per_cta * 32, cfg.smem_bytes, stream>>>(p);

@@ -4,6 +4,12 @@
 
 #include <stdint.h>
 
+#ifdef __CUDACC__
+#define GEMV_HD __host__ __device__
+#else
+#define GEMV_HD
+#endif
+
 namespace gemvk {
 
 // Fused epilogue applied to each row total before the single rounding:
@@ -35,6 +41,10 @@ struct Params {
   int32_t flags;      // kFlag* bits | (L2 prefetch rounds << kFlagL2Shift)
   Epilogue ep;
   // Tiles kernel: sw = S (warps per row, slices), nrb = C (CTAs per k-segment).
+  // Bulk kernel only:
+  int32_t stages;      // ring buffers per warp
+  int32_t wait_polls;  // mbarrier polls per ring wait before giving up
+  uint32_t *timeouts;  // per-device counter of ring waits that gave up
 };
 
 typedef void (*MainKernel)(Params);
@@ -51,6 +61,10 @@ MainKernel main_kernel_bf16(int out_f32, int variant, int R);
 // epi = 1 selects the copy built with the fused epilogue.
 MainKernel tiles_kernel_f16(int out_f32, int aligned, int R, int U, int epi);
 MainKernel tiles_kernel_bf16(int out_f32, int aligned, int R, int U, int epi);
+// Bulk kernel (B staged through shared memory by bulk async copies): R = 1,
+// unroll U in {4, 8} (32*U 16-byte blocks per ring buffer).
+MainKernel bulk_kernel_f16(int out_f32, int aligned, int U, int epi);
+MainKernel bulk_kernel_bf16(int out_f32, int aligned, int U, int epi);
 ReduceKernel reduce_kernel_f16(int out_f32);
 ReduceKernel reduce_kernel_bf16(int out_f32);
 ProbeKernel probe_kernel();
@@ -63,5 +77,15 @@ constexpr int kFlagPrefetchB = 1;
 constexpr int kFlagL2Shift = 1;  // 2 bits: tile rounds of bulk L2 prefetch ahead
 constexpr int kFlagPrefetchA = 8;   // stage a before waiting on the predecessor
 constexpr int kFlagEpilogue = 16;   // the fused epilogue is not the identity
+constexpr int kWaitPolls = 1 << 20;  // default bound on the polls of one mbarrier wait
+
+// Shared-memory layout of the bulk kernel, in bytes from the start of the
+// dynamic allocation: staged a (as_elems * 2), slice partials (2 * W
+// floats), then at a 128-byte boundary the W rings of `stages` buffers of
+// 32 * U 16-byte blocks, then one 8-byte mbarrier per buffer.
+GEMV_HD inline int64_t bulk_ring_offset(int64_t as_elems, int W) { return (as_elems * 2 + 8 * W + 127) / 128 * 128; }
+GEMV_HD inline int64_t bulk_smem_bytes(int64_t as_elems, int W, int U, int stages) {
+  return bulk_ring_offset(as_elems, W) + (int64_t)W * stages * (512 * U + 8);
+}
 
 }  // namespace gemvk

@@ -28,6 +28,8 @@ def replay(n, k, cfg, base_off=0, ldb=None):
     ldb = k if ldb is None else ldb
     if cfg["variant"] == 3:
         return replay_tiles(n, k, cfg, base_off, ldb)
+    if cfg["variant"] == 4:
+        return replay_bulk(n, k, cfg, base_off, ldb)
     assert ldb == k, "row-per-warp replay models ldb == k only"
     W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
     nrb, kseg, variant, ctas = cfg["row_blocks"], cfg["k_segment"], cfg["variant"], cfg["ctas"]
@@ -188,6 +190,140 @@ def replay_tiles(n, k, cfg, base_off=0, ldb=None):
                     np.add.at(cover[i], j0 + col_B[valid], 1)
                     if Sg > 1:
                         ws_rows.add(gs * n + i)
+    assert (cover == 1).all(), f"coverage wrong: min {cover.min()} max {cover.max()}"
+    if Sg > 1:
+        assert len(ws_rows) == Sg * n
+    return {"ctas": ctas}
+
+
+def replay_bulk(n, k, cfg, base_off=0, ldb=None):
+    """The same checks for ``gemv_bulk_kernel``, plus its ring: lane 0's
+    issue cursor and the warp's consume cursor are replayed side by side, so
+    that every bulk copy is checked (source blocks inside B, 16-byte aligned,
+    size a multiple of 16 and at most one buffer; destination inside the
+    warp's own ring; mbarrier inside shared memory), every buffer is refilled
+    only after it was consumed, every wait uses the parity of the phase that
+    the chunk it expects completes, and the consumed chunks cover each row
+    slice exactly once."""
+    ldb = k if ldb is None else ldb
+    W, R, S, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
+    C, kseg, U, ctas, NS = cfg["row_blocks"], cfg["k_segment"], cfg["unroll"], cfg["ctas"], cfg["stages"]
+    aligned = base_off == 0 and k % 8 == 0 and ldb % 8 == 0
+    NCLS = 1 if aligned else 8
+    assert R == 1 and U in (4, 8) and 2 <= NS <= 8
+    assert ctas == C * Sg and W % S == 0 and C % NCLS == 0 and C >= NCLS
+    SB = 32 * U
+    as_elems = -(-(kseg + 24) // 8) * 8
+    ring_off = -(-(as_elems * 2 + 8 * W) // 128) * 128
+    ring_bytes = W * NS * SB * 16
+    smem = cfg["smem_bytes"]
+    assert smem == ring_off + W * NS * (512 * U + 8) and smem <= 232448
+    assert as_elems * 2 + 2 * W * 4 <= ring_off  # a and the partials end before the rings
+    slots = W // S
+    if S > 1:
+        assert slots <= 15  # named barrier ids 1..slots
+    cover = np.zeros((n, k), dtype=np.int32)
+    nblocks = -(-(base_off + (n - 1) * ldb + k) // 8)
+    Cq = C // NCLS
+    ws_rows = set()
+    for cta in range(ctas):
+        gs, c = cta % Sg, cta // Sg
+        cls, cq = c % NCLS, c // NCLS
+        j0 = gs * kseg
+        seglen = min(k - j0, kseg)
+        assert seglen >= 1
+        nr = (n - cls + NCLS - 1) // NCLS if n > cls else 0
+        off = 0 if aligned else (base_off + j0 + cls * (ldb & 7)) & 7
+        nt = (off + seglen + 7) >> 3
+        last_hi = seglen + off - 8 * (nt - 1)
+        assert 1 <= last_hi <= 8 and nt <= as_elems // 8
+        RT = slots
+        L = -(-nt // S)
+        nloc = -(-(nr - cq) // Cq) if nr > cq else 0
+        ngroups = -(-nloc // RT)
+        stage_col = np.arange(8 * nt) - off
+
+        def row_of(m):
+            return NCLS * (cq + Cq * m) + cls
+
+        for warp in range(W):
+            slot, s = divmod(warp, S)
+            t0 = min(s * L, nt)
+            t1 = min(t0 + L, nt)
+            nst = -(-(t1 - t0) // SB)
+            gv = -(-(nloc - slot) // RT) if nloc > slot else 0
+            total = gv * nst
+            bufs = [None] * NS      # chunk held (or in flight) per buffer
+            phases = [0] * NS       # phases completed per buffer once its copy lands
+            cur = {"ic": 0, "ig": 0, "ist": 0, "ib": 0}
+
+            def issue():
+                ib, ig, ist = cur["ib"], cur["ig"], cur["ist"]
+                assert bufs[ib] is None, "buffer refilled before it was consumed"
+                tb = t0 + ist * SB
+                nb = min(SB, t1 - tb)
+                assert 1 <= nb <= SB
+                i = row_of(ig * RT + slot)
+                e0 = base_off + i * ldb + j0
+                assert (e0 & 7) == off
+                src = (e0 >> 3) + tb
+                assert 0 <= src and src + nb <= nblocks
+                dst = ring_off + (warp * NS + ib) * SB * 16
+                assert dst % 16 == 0 and dst + nb * 16 <= ring_off + ring_bytes
+                assert ring_off + (warp * NS + ib) * SB * 16 + SB * 16 <= ring_off + ring_bytes
+                bar = ring_off + ring_bytes + (warp * NS + ib) * 8
+                assert bar % 8 == 0 and bar + 8 <= smem
+                bufs[ib] = (cur["ic"], ig, ist, src, nb)
+                cur["ic"] += 1
+                cur["ib"] = (ib + 1) % NS
+                cur["ist"] += 1
+                if cur["ist"] == nst:
+                    cur["ist"] = 0
+                    cur["ig"] += 1
+
+            while cur["ic"] < total and cur["ic"] < NS:
+                issue()
+            cb, cpar, consumed = 0, 0, 0
+            for g in range(ngroups):
+                if g >= gv:
+                    continue
+                i = row_of(g * RT + slot)
+                assert i < n
+                for st in range(nst):
+                    held = bufs[cb]
+                    assert held is not None and held[1] == g and held[2] == st, "buffer holds the wrong chunk"
+                    cidx, _, _, src, nb = held
+                    assert cidx == consumed
+                    # the wait on parity cpar completes with this chunk's phase
+                    assert (phases[cb] & 1) == cpar
+                    phases[cb] += 1
+                    tb = t0 + st * SB
+                    assert nb == min(SB, t1 - tb)
+                    t = np.arange(tb, tb + nb)
+                    blk = src + np.arange(nb)
+                    p = np.arange(8)[None, :]
+                    tt = t[:, None]
+                    if aligned:
+                        valid = np.ones((t.size, 8), bool)
+                    else:
+                        valid = ((tt > 0) | (p >= off)) & ((tt < nt - 1) | (p < last_hi))
+                    elem = 8 * blk[:, None] + p - base_off
+                    col_B = elem - i * ldb - j0
+                    col_stage = stage_col[8 * tt + p]
+                    assert (col_B[valid] == col_stage[valid]).all()
+                    assert ((col_stage[~valid] < 0) | (col_stage[~valid] >= seglen)).all()
+                    np.add.at(cover[i], j0 + col_B[valid], 1)
+                    bufs[cb] = None
+                    consumed += 1
+                    if cur["ic"] < total:
+                        assert cur["ib"] == cb  # the refill goes into the buffer just consumed
+                        issue()
+                    cb += 1
+                    if cb == NS:
+                        cb, cpar = 0, cpar ^ 1
+                if Sg > 1:
+                    ws_rows.add(gs * n + i)
+            assert cur["ic"] == total == consumed
     assert (cover == 1).all(), f"coverage wrong: min {cover.min()} max {cover.max()}"
     if Sg > 1:
         assert len(ws_rows) == Sg * n

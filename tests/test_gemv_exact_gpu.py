@@ -28,7 +28,9 @@ CONFIGS = [None, {"variant": 2}, {"rows_per_warp": 4}, {"warps_per_cta": 4, "war
            {"variant": 3}, {"variant": 3, "warp_split": 4}, {"variant": 3, "rows_per_warp": 4, "unroll": 2},
            {"variant": 3, "rows_per_warp": 2, "unroll": 4, "warps_per_cta": 8},
            {"variant": 3, "grid_split": 3, "warp_split": 2}, {"variant": 3, "ctas": 8},
-           {"variant": 3, "l2_prefetch": 2}, {"variant": 3, "l2_prefetch": 1, "warp_split": 4, "overlap": 2}]
+           {"variant": 3, "l2_prefetch": 2}, {"variant": 3, "l2_prefetch": 1, "warp_split": 4, "overlap": 2},
+           {"variant": 4}, {"variant": 4, "stages": 2, "unroll": 4, "warp_split": 2},
+           {"variant": 4, "grid_split": 3, "warps_per_cta": 8, "warp_split": 4, "overlap": 2}]
 
 
 def _run(B, a, out_fp32=False, config=None, c=None):
@@ -92,7 +94,7 @@ TAIL_K = [1, 2, 5, 8, 9, 15, 16, 17, 31, 33, 255, 256, 257, 4099]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("variant", [None, 3])
+@pytest.mark.parametrize("variant", [None, 3, 4])
 def test_ragged_tails_bit_exact(cuda_dev, dtype, variant):
     cfg = {"variant": variant} if variant else None
     for n, k in itertools.product(TAIL_N, TAIL_K):
@@ -120,6 +122,8 @@ def test_offset_views_take_the_general_path(cuda_dev, dtype, b_off, a_off):
         assert exact_bits_match(c, Bi, ai, False), (n, k, b_off, a_off)
         c = _run(Bv, av, False, {"variant": 3})
         assert exact_bits_match(c, Bi, ai, False), (n, k, b_off, a_off, "tiles")
+        c = _run(Bv, av, False, {"variant": 4})
+        assert exact_bits_match(c, Bi, ai, False), (n, k, b_off, a_off, "bulk")
         Bu, au = inputs.make_inputs(n, k, dtype, "uniform", 9, cuda_dev)
         Bv.copy_(Bu)
         av.copy_(au)
@@ -196,7 +200,8 @@ def test_determinism_repeated_calls(cuda_dev):
     """Fixed-order reductions: 200 calls give bitwise-identical results (a
     race in the cross-warp or split-K combination would show up here)."""
     for cfg in (None, {"warp_split": 8, "warps_per_cta": 16}, {"grid_split": 4},
-                {"variant": 3, "warp_split": 4}, {"variant": 3, "grid_split": 2, "warp_split": 8}):
+                {"variant": 3, "warp_split": 4}, {"variant": 3, "grid_split": 2, "warp_split": 8},
+                {"variant": 4, "warp_split": 4}, {"variant": 4, "grid_split": 2, "warp_split": 8, "stages": 2}):
         B, a = inputs.make_inputs(3001, 5000, "f16", "normal", 2, cuda_dev, b_sigma=0.5)
         first = _run(B, a, True, cfg).clone()
         c = torch.empty_like(first)
@@ -265,7 +270,7 @@ def test_host_overhead_per_call(cuda_dev):
 
 
 @pytest.mark.parametrize("overlap", [1, 2])
-@pytest.mark.parametrize("variant", [None, 3])
+@pytest.mark.parametrize("variant", [None, 3, 4])
 def test_overlap_respects_dependencies(cuda_dev, overlap, variant):
     """Programmatic dependent launch: each call still sees the memory of the
     kernels before it.  A chain x_{m+1} = B @ x_m (c of one call is a of the
@@ -301,7 +306,7 @@ def test_overlap_respects_dependencies(cuda_dev, overlap, variant):
     check_against_oracle(c, B2, xs[0], False, label="WAW on c")
 
 
-@pytest.mark.parametrize("variant", [None, 3])
+@pytest.mark.parametrize("variant", [None, 3, 4])
 def test_overlap_pdl_sees_rewritten_B(cuda_dev, variant):
     """GEMV_OVERLAP_PDL (without the B prefetch) also orders B: a kernel that
     rewrites B right before the call is waited for."""
@@ -329,7 +334,7 @@ def test_overlap_uses_cached_plan(cuda_dev):
     assert ei.value.status == g.GEMV_ERR_CONFIG
 
 
-@pytest.mark.parametrize("variant", [None, 3, 1])
+@pytest.mark.parametrize("variant", [None, 3, 1, 4])
 def test_overlap_prefetch_ba_shared_input(cuda_dev, variant):
     """GEMV_OVERLAP_PDL_PREFETCH_BA (B and a promised unwritten by the work in
     flight): several GEMVs on one input vector, e.g. the projections of one

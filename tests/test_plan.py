@@ -67,7 +67,7 @@ def test_forced_configs_are_honoured(gemv_lib, cfg):
 
 
 @pytest.mark.parametrize("cfg", [
-    {"variant": 4}, {"rows_per_warp": 3}, {"warps_per_cta": 12}, {"warps_per_cta": 8, "warp_split": 3},
+    {"variant": 5}, {"rows_per_warp": 3}, {"warps_per_cta": 12}, {"warps_per_cta": 8, "warp_split": 3},
     {"grid_split": 65}, {"variant": 2, "rows_per_warp": 2}, {"rows_per_warp": 2, "unroll": 8},
 ])
 def test_invalid_forced_configs_rejected(gemv_lib, cfg):
@@ -205,3 +205,83 @@ def test_tiles_index_replay_strided(gemv_lib, n, k, ldb, base_off, forced):
                                          (2, 100, 1024, 4), (4, 256, 24, 2), (1, 0, 64, 2)])
 def test_gla_index_replay(bh, dk, dv, es):
     kernel_model.replay_gla(bh, dk, dv, es)
+
+
+# ------------------------------------------------------------- bulk variant --
+
+BULK_FORCED = [{}, {"stages": 2}, {"stages": 3, "unroll": 4}, {"unroll": 8, "stages": 2}, {"warp_split": 2},
+               {"warps_per_cta": 8, "warp_split": 4, "stages": 3}, {"grid_split": 3}, {"ctas": 8},
+               {"warps_per_cta": 4, "warp_split": 2, "grid_split": 2, "stages": 5}, {"stages": 8, "unroll": 4}]
+
+
+@pytest.mark.parametrize("n,k", [(1, 1), (3, 9), (17, 7), (64, 512), (33, 1000), (9, 5000), (40, 4099),
+                                 (5, 16384), (2, 33000), (300, 24), (130, 2056)])
+@pytest.mark.parametrize("base_off", [0, 1, 6])
+@pytest.mark.parametrize("forced", BULK_FORCED)
+def test_bulk_index_replay(gemv_lib, n, k, base_off, forced):
+    """Ring replay of the bulk kernel: several chunks per row slice, rings that
+    wrap, unaligned rows, split-K."""
+    cfg_in = dict(forced)
+    cfg_in["variant"] = 4
+    aligned = base_off == 0
+    try:
+        cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config=cfg_in)
+    except gemv_lib.GemvError:
+        pytest.skip("configuration not valid for this shape")
+    assert cfg["variant"] == 4 and cfg["rows_per_warp"] == 1
+    for key in ("stages", "unroll", "warp_split", "warps_per_cta"):
+        if key in forced:
+            assert cfg[key] == forced[key]
+    kernel_model.replay(n, k, cfg, base_off=base_off)
+
+
+@pytest.mark.parametrize("n,k,ldb", [(5, 17, 24), (9, 64, 67), (17, 7, 8), (3, 4099, 5000), (7, 1000, 1003),
+                                     (6, 3000, 3008)])
+@pytest.mark.parametrize("base_off", [0, 3])
+@pytest.mark.parametrize("forced", [{}, {"warp_split": 2, "stages": 2}, {"grid_split": 3}])
+def test_bulk_index_replay_strided(gemv_lib, n, k, ldb, base_off, forced):
+    cfg_in = dict(forced)
+    cfg_in["variant"] = 4
+    aligned = base_off == 0 and ldb % 8 == 0
+    try:
+        cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config=cfg_in)
+    except gemv_lib.GemvError:
+        pytest.skip("configuration not valid for this shape")
+    kernel_model.replay(n, k, cfg, base_off=base_off, ldb=ldb)
+
+
+@pytest.mark.parametrize("n,k", WORKLOADS)
+@pytest.mark.parametrize("aligned", [True, False])
+def test_bulk_plan_invariants(gemv_lib, n, k, aligned):
+    cfg = gemv_lib.gemv_plan(n, k, 1, aligned, SM, config={"variant": 4})
+    W, S, C, Sg, U, NS = (cfg[x] for x in ("warps_per_cta", "warp_split", "row_blocks", "grid_split", "unroll",
+                                            "stages"))
+    ncls = 1 if aligned and k % 8 == 0 else 8
+    assert cfg["variant"] == 4 and cfg["rows_per_warp"] == 1 and U in (4, 8) and 2 <= NS <= 4
+    assert W % S == 0 and C % ncls == 0 and C >= ncls and cfg["ctas"] == C * Sg
+    assert Sg * cfg["k_segment"] >= k and (Sg - 1) * cfg["k_segment"] < k
+    as_elems = -(-(cfg["k_segment"] + 24) // 8) * 8
+    ring_off = -(-(as_elems * 2 + 8 * W) // 128) * 128
+    assert cfg["smem_bytes"] == ring_off + W * NS * (512 * U + 8) <= MAX_SMEM
+    # the planner takes the deepest ring (at most 4) that fits
+    if NS < 4:
+        assert ring_off + W * (NS + 1) * (512 * U + 8) > MAX_SMEM
+    assert cfg["l2_prefetch"] == 0
+    # never more CTAs than are resident at once
+    cps = min(32 // W, 233472 // (cfg["smem_bytes"] + 1024))
+    assert cfg["ctas"] <= max(SM * cps, Sg * ncls)
+
+
+@pytest.mark.parametrize("cfg", [{"variant": 4, "rows_per_warp": 2}, {"variant": 4, "unroll": 2},
+                                 {"variant": 4, "stages": 1}, {"variant": 4, "stages": 9},
+                                 {"variant": 4, "l2_prefetch": 1}, {"variant": 3, "stages": 2},
+                                 {"variant": 1, "stages": 2}, {"stages": 3}])
+def test_bulk_invalid_configs_rejected(gemv_lib, cfg):
+    with pytest.raises(gemv_lib.GemvError) as ei:
+        gemv_lib.gemv_plan(4096, 4096, 0, True, SM, config=cfg)
+    assert ei.value.status == gemv_lib.GEMV_ERR_CONFIG
+
+
+def test_bulk_is_never_chosen_automatically(gemv_lib):
+    for n, k in WORKLOADS:
+        assert gemv_lib.gemv_plan(n, k, 0, True, SM)["variant"] != 4
