@@ -86,19 +86,31 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources that make up the device code of the streaming GEMV kernels (the
+# tiles and bulk kernels, their shared helpers and their instantiations).
+KERNEL_SOURCES = ("gemv_internal.h", "gemv_kernels.cuh", "gemv_tiles.cuh", "gemv_bulk.cuh",
+                  "gemv_kernels_f16.cu", "gemv_kernels_bf16.cu", "gemv_bulk_f16.cu", "gemv_bulk_bf16.cu")
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_bound_gemv_02_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_tag: str):
+def launch_signature(cfg: dict) -> str:
+    """The launch configuration a profile was taken with."""
+    return " ".join(f"{kk}={cfg[kk]}" for kk in ("variant", "rows_per_warp", "unroll", "warps_per_cta",
+                                                 "warp_split", "grid_split", "ctas", "stages"))
+
+
+def profiled_traffic(workload_tag: str, cfg: dict):
     """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel sources (else None)."""
+    if it was taken on the current kernel sources and the launch
+    configuration ``cfg`` (else None)."""
     path = os.path.join(ROOT, "profiles", f"gemv_{workload_tag}.md")
     try:
         lines = open(path).read().splitlines()
@@ -109,7 +121,7 @@ def profiled_traffic(workload_tag: str):
         if line.startswith("- ") and ":" in line:
             key, _, v = line[2:].partition(":")
             vals[key.strip()] = v.strip().strip("`")
-    if vals.get("source_digest") != kernel_source_digest():
+    if vals.get("source_digest") != kernel_source_digest() or vals.get("launch") != launch_signature(cfg):
         return None
     try:
         return int(vals["dram_bytes_per_launch"])
@@ -378,10 +390,11 @@ def host_overhead_us(L, n, k, dt, dev, stream):
     return statistics.median(per) * 1e6
 
 
-def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev):
+def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, variant=0):
     """One shape: µs per call three ways -- isolated (CUDA events around each
     launch), back to back, and back to back with programmatic dependent
-    launch -- and the launch configuration."""
+    launch -- and the launch configuration.  ``variant``: a GEMV_VARIANT_*
+    forced on every call (0: the planner's choice)."""
     import torch
 
     from memory_bound_gemv_02_gb300 import inputs
@@ -393,10 +406,17 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev):
     c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
     dt = g.dtype_code(B.dtype, out_fp32)
     s = torch.cuda.current_stream().cuda_stream
-    g.gemv(B, a, c=c, out_fp32=out_fp32)
+    fc = g.GemvConfig()
+    fc.variant = variant
+    g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=fc)
     cfg = g.gemv_last_config()
-    plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in Bs]
+    if variant:
+        plain = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(fc), s))
+                 for Bx in Bs]
+    else:
+        plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in Bs]
     ov = g.GemvConfig()
+    ov.variant = variant
     ov.overlap = g.GEMV_OVERLAP_PDL_PREFETCH_B
     pdl = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(ov), s)) for Bx in Bs]
     _, per = time_calls(L, plain, s, steps, warmup)
@@ -413,7 +433,7 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev):
             "gbs_isolated": round(nbytes / iso / 1e3, 1), "gbs_back_to_back": round(nbytes / b2b / 1e3, 1),
             "gbs_back_to_back_pdl": round(nbytes / b2b_pdl / 1e3, 1),
             "config": {kk: cfg[kk] for kk in ("variant", "rows_per_warp", "unroll", "warps_per_cta",
-                                              "warp_split", "grid_split", "ctas")}}
+                                              "warp_split", "grid_split", "ctas", "stages")}}
 
 
 def run_sweep(args, dev):
@@ -427,6 +447,11 @@ def run_sweep(args, dev):
         r = bench_shape(g, L, n, k, dtype, out_fp32, dist, 0, args.sweep_steps, 20, dev)
         r["pct_of_8tbps_pdl"] = round(100 * r["gbs_back_to_back_pdl"] / NOMINAL_HBM_GBS, 1)
         r[f"frac_of_{kind}_peak_pdl"] = round(r["gbs_back_to_back_pdl"] / peak, 4)
+        # the same shape with B staged through shared memory (bulk variant)
+        rb = bench_shape(g, L, n, k, dtype, out_fp32, dist, 0, args.sweep_steps, 20, dev,
+                         variant=g.GEMV_VARIANT_BULK)
+        r["bulk"] = {kk: rb[kk] for kk in ("us_isolated_median", "us_back_to_back", "us_back_to_back_pdl",
+                                           "gbs_back_to_back_pdl", "config")}
         out.write(json.dumps(r) + "\n")
         out.flush()
         print(json.dumps(r), file=sys.stderr, flush=True)
@@ -642,7 +667,7 @@ def run_ours(args, world, rank, local):
         "pct_of_nominal_8tbps": round(100 * achieved / NOMINAL_HBM_GBS, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(frac_of_peak(achieved, peak), 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": profiled_traffic("7168x16384_f16")},
+                     "traffic": profiled_traffic("7168x16384_f16", cfg)},
         "probe_read_gbs": round(probe_gbs, 1),
         "host_us_per_call": round(host_us, 3),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",

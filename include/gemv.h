@@ -78,7 +78,9 @@ enum {
                                     completion tracked by one mbarrier per buffer.  The
                                     sm_103a form of the multi-stage shared-memory pipeline of
                                     B (TileLang Case Studies, Case B.1 "O3 Pipelined B
-                                    Loads"); chosen only when forced */
+                                    Loads").  The planner picks it for B of 512 MiB or more
+                                    (192 MiB or more when rows are not 16-byte aligned) when
+                                    at most 2 warps share a row; otherwise only when forced */
 };
 
 /* Launch overlap with the preceding work on the stream (gemv_config.overlap). */
@@ -134,8 +136,7 @@ enum {
  *                 ahead (one bulk prefetch per row slice; 0 = none, at most
  *                 3; -1 forces 0 when forcing).
  *  stages         bulk variant: buffers in each warp's ring (2 .. 8; the
- *                 planner takes the most of 4, 3, 2 that fit in shared
- *                 memory).  0 for the other variants.
+ *                 planner takes 2).  0 for the other variants.
  */
 typedef struct gemv_config {
   int32_t variant;

@@ -33,6 +33,9 @@ constexpr int64_t kMaxSegment = 32768;  // columns of a staged per CTA (64 KiB o
 constexpr int kMaxGridSplit = 64;
 constexpr int kAutoVariant = GEMV_VARIANT_TILES;  // the planner's default family
 constexpr int kDefaultL2Prefetch = 0;              // tile rounds of L2 prefetch by default
+constexpr int kBulkDefaultStages = 2;              // ring buffers per warp of the bulk variant
+constexpr int64_t kBulkAutoBytes = 512LL << 20;    // B bytes from which the planner picks the bulk variant
+constexpr int64_t kBulkAutoBytesUnaligned = 192LL << 20;  // the same, rows not 16-byte aligned
 constexpr int kMaxSmemPerCta = 232448;  // 227 KiB, sm_100-family opt-in limit
 constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int64_t kSmemReservedPerCta = 1024;
@@ -211,8 +214,11 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
         NS = f->stages;
         if (NS < 2 || NS > 8) return GEMV_ERR_CONFIG;
       } else {
-        for (NS = 4; NS > 2 && bulk_smem_bytes(as_elems, W, U, NS) > kMaxSmemPerCta; --NS) {
-        }
+        // Two buffers per warp: 16 warps x 2 x 4 KiB in flight per SM, as
+        // many bytes as the register kernel keeps in flight.  Deeper rings
+        // measured slower on GB300 (7168 x 16384: 36.3 us with 2, 36.7 with
+        // 3; 28672 x 8192: 66.6 vs 70.1 us).
+        NS = kBulkDefaultStages;
       }
     } else if (f->stages) {
       return GEMV_ERR_CONFIG;
@@ -257,10 +263,6 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     c.grid_split = (int32_t)Sg;
     c.row_blocks = (int32_t)C;
     c.ctas = (int32_t)(C * Sg);
-    if (bulk && !f->stages) {
-      // A shorter final segment may leave room for a deeper ring.
-      while (NS < 4 && bulk_smem_bytes(round_up(kseg + 24, 8), W, U, NS + 1) <= kMaxSmemPerCta) ++NS;
-    }
     c.smem_bytes = (int32_t)(bulk ? bulk_smem_bytes(round_up(kseg + 24, 8), W, U, NS)
                                   : round_up(kseg + 24, 8) * 2 + 2LL * W * R * 4);
     c.stages = NS;
@@ -281,17 +283,36 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
   return GEMV_OK;
 }
 
+bool is_unforced(const gemv_config &f) {
+  return !(f.variant || f.rows_per_warp || f.warps_per_cta || f.warp_split || f.grid_split || f.ctas ||
+           f.unroll || f.l2_prefetch || f.stages);
+}
+
 // The planner.  Pure host arithmetic: no CUDA call.
 int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_config *f,
               gemv_config *out) {
   if (dtype < 0 || dtype > 3) return GEMV_ERR_DTYPE;
   if (n < 1 || k < 1 || k > INT32_MAX || sm < 1) return GEMV_ERR_ARG;
   gemv_config fz{};
-  if (f == nullptr) f = &fz;
+  if (f == nullptr || is_unforced(*f)) f = &fz;
 
   const int auto_variant = (kAutoVariant == GEMV_VARIANT_ROWS && !aligned) ? GEMV_VARIANT_ROWS_GENERAL
                                                                             : kAutoVariant;
   const int variant = f->variant ? f->variant : auto_variant;
+  if (variant == GEMV_VARIANT_TILES && f == &fz) {
+    // Nothing forced: the tiles plan, or the bulk variant with the same work
+    // split where it measured faster on GB300 (B of 512 MiB or more -- 192
+    // MiB or more when the rows are not 16-byte aligned -- streamed by at
+    // most 2 warps per row: 57344 x 7168 116.8 -> 114.5 us, 65536 x 7169
+    // 139.6 -> 134.5 us, 16384 x 7169 38.8 -> 37.7 us back to back).
+    int st = plan_tiles(n, k, aligned, sm, f, out);
+    const int64_t b_bytes = n * k * 2;
+    if (st == GEMV_OK && out->warp_split <= 2 && b_bytes >= (aligned ? kBulkAutoBytes : kBulkAutoBytesUnaligned)) {
+      gemv_config b{};
+      if (plan_tiles(n, k, aligned, sm, f, &b, true) == GEMV_OK && b.warp_split <= 2) *out = b;
+    }
+    return st;
+  }
   if (variant == GEMV_VARIANT_TILES) return plan_tiles(n, k, aligned, sm, f, out);
   if (variant == GEMV_VARIANT_BULK) return plan_tiles(n, k, aligned, sm, f, out, true);
   if (f->stages) return GEMV_ERR_CONFIG;

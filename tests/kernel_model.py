@@ -222,7 +222,7 @@ def replay_bulk(n, k, cfg, base_off=0, ldb=None):
     slots = W // S
     if S > 1:
         assert slots <= 15  # named barrier ids 1..slots
-    cover = np.zeros((n, k), dtype=np.int32)
+    cover = np.zeros((n, k), dtype=np.uint8)  # 0 or 1 expected; uint8 keeps full-size replays small
     nblocks = -(-(base_off + (n - 1) * ldb + k) // 8)
     Cq = C // NCLS
     ws_rows = set()

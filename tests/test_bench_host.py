@@ -58,3 +58,20 @@ def test_reference_arm_line(tmp_path):
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["higher_is_better"] is True
+
+
+def test_profiled_traffic_gated_by_sources_and_launch(gemv_lib):
+    """The roofline's `traffic` comes from the committed ncu summary only
+    while the kernel sources and the launch configuration are the ones it
+    was captured with."""
+    cfg = gemv_lib.gemv_plan(7168, 16384, 0, True, 152)
+    got = bench.profiled_traffic("7168x16384_f16", cfg)
+    text = open(os.path.join(bench.ROOT, "profiles", "gemv_7168x16384_f16.md")).read()
+    if f"source_digest: `{bench.kernel_source_digest()}`" in text:
+        assert isinstance(got, int) and 234_928_128 <= got < 234_928_128 * 1.05
+    else:
+        assert got is None
+    other = dict(cfg, warp_split=cfg["warp_split"] * 2)
+    assert bench.profiled_traffic("7168x16384_f16", other) is None
+    assert bench.profiled_traffic("no_such_workload", cfg) is None
+    assert bench.launch_signature(cfg).startswith("variant=3 ")

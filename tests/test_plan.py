@@ -26,7 +26,7 @@ def test_plan_invariants(gemv_lib, n, k, dtype, aligned, sm):
     cfg = gemv_lib.gemv_plan(n, k, dtype, aligned, sm)
     W, R, Sw, Sg = cfg["warps_per_cta"], cfg["rows_per_warp"], cfg["warp_split"], cfg["grid_split"]
     assert W in (4, 8, 16) and R in (1, 2, 4) and W % Sw == 0
-    assert cfg["variant"] == 3
+    assert cfg["variant"] in (3, 4)
     kseg = cfg["k_segment"]
     assert Sg * kseg >= k and (Sg - 1) * kseg < k
     if Sg > 1:
@@ -257,15 +257,12 @@ def test_bulk_plan_invariants(gemv_lib, n, k, aligned):
     W, S, C, Sg, U, NS = (cfg[x] for x in ("warps_per_cta", "warp_split", "row_blocks", "grid_split", "unroll",
                                             "stages"))
     ncls = 1 if aligned and k % 8 == 0 else 8
-    assert cfg["variant"] == 4 and cfg["rows_per_warp"] == 1 and U in (4, 8) and 2 <= NS <= 4
+    assert cfg["variant"] == 4 and cfg["rows_per_warp"] == 1 and U in (4, 8) and NS == 2
     assert W % S == 0 and C % ncls == 0 and C >= ncls and cfg["ctas"] == C * Sg
     assert Sg * cfg["k_segment"] >= k and (Sg - 1) * cfg["k_segment"] < k
     as_elems = -(-(cfg["k_segment"] + 24) // 8) * 8
     ring_off = -(-(as_elems * 2 + 8 * W) // 128) * 128
     assert cfg["smem_bytes"] == ring_off + W * NS * (512 * U + 8) <= MAX_SMEM
-    # the planner takes the deepest ring (at most 4) that fits
-    if NS < 4:
-        assert ring_off + W * (NS + 1) * (512 * U + 8) > MAX_SMEM
     assert cfg["l2_prefetch"] == 0
     # never more CTAs than are resident at once
     cps = min(32 // W, 233472 // (cfg["smem_bytes"] + 1024))
@@ -282,6 +279,32 @@ def test_bulk_invalid_configs_rejected(gemv_lib, cfg):
     assert ei.value.status == gemv_lib.GEMV_ERR_CONFIG
 
 
-def test_bulk_is_never_chosen_automatically(gemv_lib):
-    for n, k in WORKLOADS:
-        assert gemv_lib.gemv_plan(n, k, 0, True, SM)["variant"] != 4
+@pytest.mark.parametrize("aligned", [True, False])
+def test_bulk_auto_choice(gemv_lib, aligned):
+    """Unforced plans use the bulk variant exactly for B of at least 512 MiB
+    (192 MiB for unaligned rows) split over at most 2 warps per row, with the
+    tiles plan's work split; everything else is the tiles plan."""
+    for n, k in WORKLOADS + [(65536, 7169), (16384, 7169), (18432, 7168), (65536, 16384)]:
+        auto = gemv_lib.gemv_plan(n, k, 0, aligned, SM)
+        tiles = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 3})
+        al = aligned and k % 8 == 0
+        big = n * k * 2 >= (512 << 20 if al else 192 << 20)
+        if big and tiles["warp_split"] <= 2:
+            assert auto["variant"] == 4, (n, k, aligned)
+            assert auto == gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 4})
+            assert auto["warp_split"] == tiles["warp_split"] and auto["grid_split"] == tiles["grid_split"]
+        else:
+            assert auto == tiles, (n, k, aligned)
+    assert gemv_lib.gemv_plan(57344, 7168, 1, True, SM)["variant"] == 4
+    assert gemv_lib.gemv_plan(16384, 7169, 0, False, SM)["variant"] == 4
+    assert gemv_lib.gemv_plan(7168, 16384, 0, True, SM)["variant"] == 3
+    assert gemv_lib.gemv_plan(18432, 7168, 1, True, SM)["variant"] == 3
+
+
+@pytest.mark.parametrize("n,k,base_off", [(16384, 7169, 0)])
+def test_bulk_auto_plans_replay(gemv_lib, n, k, base_off):
+    """An automatic bulk plan of a workload shape, replayed in full (every
+    CTA, warp and ring chunk)."""
+    cfg = gemv_lib.gemv_plan(n, k, 0, base_off == 0, SM)
+    assert cfg["variant"] == 4
+    kernel_model.replay(n, k, cfg, base_off=base_off)
