@@ -460,7 +460,8 @@ def run_sweep(args, dev):
     return 0
 
 
-GLA_WORKLOADS = [(2048, 128, 128, "bf16"), (2048, 128, 128, "f32"), (1024, 256, 256, "bf16"), (4096, 64, 64, "f16")]
+GLA_WORKLOADS = [(2048, 128, 128, "bf16"), (2048, 128, 128, "f32"), (1024, 256, 256, "bf16"), (4096, 64, 64, "f16"),
+                 (8192, 64, 64, "bf16"), (4096, 128, 128, "bf16"), (16384, 16, 64, "f16")]
 
 
 def run_gla(args, dev):
@@ -490,20 +491,29 @@ def run_gla(args, dev):
             q, k, v, gk, S = (x.to(tdt[dt]) for x in (q, k, v, gk, S))
             o = torch.empty((bh, dv), dtype=tdt[dt], device=dev)
             sets.append((q, k, v, gk, S, o))
-        calls = [(L.gla_decode, (q.data_ptr(), k.data_ptr(), v.data_ptr(), gk.data_ptr(), S.data_ptr(),
-                                 S.data_ptr(), o.data_ptr(), bh, dk, dv, ctypes.c_float(dk ** -0.5), code[dt], s))
-                 for q, k, v, gk, S, o in sets]
-        _, per = time_calls(L, calls, s, args.gla_steps, 10)
-        el = time_batch(calls, args.gla_steps, 10)
-        iso = statistics.median(per) * 1e3
-        b2b = el / args.gla_steps * 1e6
+        def timed(variant):
+            calls = [(L.gla_decode_ex, (q.data_ptr(), k.data_ptr(), v.data_ptr(), gk.data_ptr(), S.data_ptr(),
+                                        S.data_ptr(), o.data_ptr(), bh, dk, dv, ctypes.c_float(dk ** -0.5),
+                                        code[dt], variant, s))
+                     for q, k, v, gk, S, o in sets]
+            if calls[0][0](*calls[0][1]) != 0:
+                return None
+            _, per = time_calls(L, calls, s, args.gla_steps, 10)
+            el = time_batch(calls, args.gla_steps, 10)
+            return statistics.median(per) * 1e3, el / args.gla_steps * 1e6
+
+        iso, b2b = timed(g.GLA_VARIANT_AUTO)
         r = {"workload": f"gla_decode bh={bh} dk={dk} dv={dv} {dt} (in place)", "bytes": nbytes,
              "us_isolated_median": round(iso, 3), "us_back_to_back": round(b2b, 3),
              "gbs_back_to_back": round(nbytes / b2b / 1e3, 1), "gbs_isolated": round(nbytes / iso / 1e3, 1),
              "pct_of_8tbps": round(100 * nbytes / b2b / 1e3 / NOMINAL_HBM_GBS, 1), "state_copies": copies}
+        # each kernel layout forced, for comparison
+        for name, variant in (("cta", g.GLA_VARIANT_CTA), ("warp", g.GLA_VARIANT_WARP)):
+            t = timed(variant)
+            r[f"us_back_to_back_{name}"] = None if t is None else round(t[1], 3)
         out.append(r)
         print(json.dumps(r), file=sys.stderr, flush=True)
-        del sets, calls
+        del sets
         torch.cuda.empty_cache()
     print(json.dumps({"gla_decode": out}), flush=True)
     return 0

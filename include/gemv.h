@@ -368,6 +368,31 @@ enum { GLA_F16 = 0, GLA_BF16 = 1, GLA_F32 = 2 };
 int gla_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
                void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, cudaStream_t stream);
 
+/* Kernel layouts of gla_decode_ex(). */
+enum {
+  GLA_VARIANT_AUTO = 0,     /* gla_decode()'s choice */
+  GLA_VARIANT_CTA = 1,      /* a CTA of 256 threads takes G heads per round (G = 1 for large heads,
+                               more for small ones: about 4 rows per thread): 16-byte column chunks
+                               of 4 rows in flight per thread, row-block partials of o added in
+                               shared memory */
+  GLA_VARIANT_WARP = 2      /* one warp per head: lanes own (row group, column chunk) pairs, 8 rows
+                               in flight per lane, o reduced by warp shuffles; needs
+                               dv * element size <= 512 bytes */
+};
+
+/*
+ * gla_decode() with the kernel layout chosen by the caller (`variant`,
+ * GLA_VARIANT_*).  The automatic choice is GLA_VARIANT_CTA, which takes
+ * several small heads side by side per round (measured faster than a warp
+ * per head on every workload tried).  GEMV_ERR_CONFIG for a layout the shape
+ * does not allow;
+ * otherwise as gla_decode().  The two layouts compute every S_new element
+ * identically; o differs only by the order of its fp32 sum.
+ */
+int gla_decode_ex(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
+                  void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, int variant,
+                  cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

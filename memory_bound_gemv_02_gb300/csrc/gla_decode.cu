@@ -7,14 +7,18 @@
 // writes it once -- bandwidth-bound like the GEMV -- and its output is a
 // transposed matrix-vector product fused into the update.
 //
-// Design: a persistent grid walks the heads.  For a head, exp(gk), k and q
-// are staged in shared memory (fp32); thread t owns the 16-byte column chunk
-// t % (dv / VEC) of rows t / (dv / VEC), t / (dv / VEC) + RP, ... (so a warp's
-// loads and stores cover contiguous rows: fully coalesced), updates each
-// element as fmaf(exp(gk_i), S_ij, k_i v_j) in fp32, stores it rounded once,
-// and accumulates q_i * S_new_ij (unrounded) for its columns.  The RP row
-// partials of each column are added in shared memory in row-block order, so
-// the result is deterministic.  Four rows are in flight per thread.
+// Design: a persistent grid walks the heads, G at a time per CTA round (G = 1
+// for large heads; small heads side by side, so that each thread still has
+// about four rows to stream).  For a round, exp(gk), k and q of its heads are
+// staged in shared memory (fp32); the threads of head slot g own, thread t of
+// the slot, the 16-byte column chunk t % (dv / VEC) of rows t / (dv / VEC),
+// t / (dv / VEC) + RP, ... (so a warp's loads and stores cover contiguous
+// rows: fully coalesced), update each element as fmaf(exp(gk_i), S_ij,
+// k_i v_j) in fp32, store it rounded once, and accumulate q_i * S_new_ij
+// (unrounded) for their columns.  The RP row partials of each column are
+// added in shared memory in row-block order, so the result is deterministic.
+// Four rows are in flight per thread; the first four are requested before
+// the round's staging, so their latency overlaps it.
 // S_new may be S itself (an in-place step): every element is read and then
 // written by the same thread.
 #include <cuda_runtime.h>
@@ -33,6 +37,7 @@ struct GlaParams {
   int64_t bh;
   int32_t dk, dv;
   float scale;
+  int32_t heads_per_cta;  // gla_decode_kernel: heads processed side by side per round (G)
 };
 
 struct F32 {};  // tag of the fp32 storage type
@@ -111,39 +116,55 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_kernel(GlaParams p) {
   using IO = GlaIo<T>;
   constexpr int VEC = IO::VEC;
   extern __shared__ float gsm[];
-  const int dk = p.dk, dv = p.dv;
-  float *dec = gsm;           // exp(gk)   [dk]
-  float *kk = dec + dk;       // k         [dk]
-  float *qq = kk + dk;        // q         [dk]
-  float *part = qq + dk;      // row-block partials of o [RP][dv]
-  const int cpr = dv / VEC;   // 16-byte chunks per row
-  const int RP = kGlaThreads / cpr;  // row blocks (>= 1: the host keeps cpr <= kGlaThreads)
+  const int dk = p.dk, dv = p.dv, G = p.heads_per_cta;
+  const int cpr = dv / VEC;               // 16-byte chunks per row
+  const int TPG = kGlaThreads / G;        // threads per head
+  const int RP = TPG / cpr;               // row blocks per head (>= 1: the host keeps G * cpr <= kGlaThreads)
+  float *dec = gsm;                       // exp(gk)   [G][dk]
+  float *kk = dec + G * dk;               // k         [G][dk]
+  float *qq = kk + G * dk;                // q         [G][dk]
+  float *part = qq + G * dk;              // row-block partials of o [G][RP][dv]
   const int t = threadIdx.x;
-  const int cc = t % cpr, rl = t / cpr;
-  const bool active = rl < RP;
+  const int gi = t / TPG, tl = t % TPG;   // head slot of this thread, its index in the slot
+  const int cc = tl % cpr, rl = tl / cpr;
+  const int64_t rounds = (p.bh + G - 1) / G;
 
-  for (int64_t h = blockIdx.x; h < p.bh; h += gridDim.x) {
-    for (int i = t; i < dk; i += kGlaThreads) {
-      dec[i] = expf(IO::scalar(p.gk, h * dk + i));
-      kk[i] = IO::scalar(p.k, h * dk + i);
-      qq[i] = IO::scalar(p.q, h * dk + i);
+  for (int64_t r = blockIdx.x; r < rounds; r += gridDim.x) {
+    const int64_t h0 = r * G;                    // first head of this round
+    const int nh = (p.bh - h0 < G) ? (int)(p.bh - h0) : G;
+    const int64_t h = h0 + gi;                   // this thread's head
+    const bool active = rl < RP && gi < nh;
+    const uint4 *Srow = reinterpret_cast<const uint4 *>(p.S) + (h * dk) * (int64_t)cpr + cc;
+    // The first rows of the head are requested before q, k, gk are staged,
+    // so that the two latencies overlap.
+    uint4 sv[kGlaRowsInFlight];
+#pragma unroll
+    for (int u = 0; u < kGlaRowsInFlight; ++u) {
+      const int i = rl + u * RP;
+      sv[u] = (active && i < dk) ? ldg_stream(Srow + (int64_t)i * cpr) : zero4();
+    }
+    for (int x = t; x < nh * dk; x += kGlaThreads) {
+      dec[x] = expf(IO::scalar(p.gk, h0 * dk + x));
+      kk[x] = IO::scalar(p.k, h0 * dk + x);
+      qq[x] = IO::scalar(p.q, h0 * dk + x);
     }
     __syncthreads();
     if (active) {
+      const float *hd = dec + gi * dk, *hk = kk + gi * dk, *hq = qq + gi * dk;
       // this thread's VEC elements of v (16-byte aligned: dv % VEC == 0)
       float vv[VEC];
       IO::unpack(__ldg(reinterpret_cast<const uint4 *>(p.v) + (h * dv) / VEC + cc), vv);
       float acc[VEC];
 #pragma unroll
       for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
-      const uint4 *Srow = reinterpret_cast<const uint4 *>(p.S) + (h * dk) * (int64_t)cpr + cc;
       uint4 *Nrow = reinterpret_cast<uint4 *>(p.S_new) + (h * dk) * (int64_t)cpr + cc;
       for (int i0 = rl; i0 < dk; i0 += RP * kGlaRowsInFlight) {
-        uint4 sv[kGlaRowsInFlight];
+        if (i0 != rl) {
 #pragma unroll
-        for (int u = 0; u < kGlaRowsInFlight; ++u) {
-          const int i = i0 + u * RP;
-          sv[u] = (i < dk) ? ldg_stream(Srow + (int64_t)i * cpr) : zero4();
+          for (int u = 0; u < kGlaRowsInFlight; ++u) {
+            const int i = i0 + u * RP;
+            sv[u] = (i < dk) ? ldg_stream(Srow + (int64_t)i * cpr) : zero4();
+          }
         }
 #pragma unroll
         for (int u = 0; u < kGlaRowsInFlight; ++u) {
@@ -151,7 +172,7 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_kernel(GlaParams p) {
           if (i < dk) {
             float s[VEC], sn[VEC];
             IO::unpack(sv[u], s);
-            const float di = dec[i], ki = kk[i], qi = qq[i];
+            const float di = hd[i], ki = hk[i], qi = hq[i];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               sn[e] = fmaf(di, s[e], ki * vv[e]);
@@ -162,15 +183,83 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_kernel(GlaParams p) {
         }
       }
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) part[rl * dv + cc * VEC + e] = acc[e];
+      for (int e = 0; e < VEC; ++e) part[(gi * RP + rl) * dv + cc * VEC + e] = acc[e];
     }
     __syncthreads();
-    for (int j = t; j < dv; j += kGlaThreads) {
+    for (int x = t; x < nh * dv; x += kGlaThreads) {
+      const int g = x / dv, j = x % dv;
       float sum = 0.f;
-      for (int r = 0; r < RP; ++r) sum += part[r * dv + j];
-      IO::store_scalar(p.o, h * dv + j, p.scale * sum);
+      for (int rb = 0; rb < RP; ++rb) sum += part[(g * RP + rb) * dv + j];
+      IO::store_scalar(p.o, h0 * dv + x, p.scale * sum);
     }
-    __syncthreads();  // dec/kk/qq/part are reused by the next head
+    __syncthreads();  // dec/kk/qq/part are reused by the next round
+  }
+}
+
+// One warp per head, for many small heads (dv * element size <= 512 bytes):
+// lane l owns 16-byte column chunk l % cpr of rows l / cpr, l / cpr + RPW,
+// ... (RPW = 32 / cpr row groups per warp), with 8 of its rows in flight,
+// their exp(gk_i), k_i, q_i loaded beside them.  No block barrier: o's
+// column sums are reduced over the RPW row groups by shuffles, in row-group
+// order (deterministic).  The update of each element is the same fmaf as in
+// gla_decode_kernel, so S_new is bit-identical between the two layouts.
+constexpr int kGlaWarpRows = 8;
+
+template <class T>
+__global__ void __launch_bounds__(kGlaThreads) gla_decode_warp_kernel(GlaParams p) {
+  using IO = GlaIo<T>;
+  constexpr int VEC = IO::VEC;
+  constexpr int RW = kGlaWarpRows;
+  const int dk = p.dk, dv = p.dv;
+  const int cpr = dv / VEC;  // <= 32 (host)
+  const int RPW = 32 / cpr;
+  const int lane = threadIdx.x & 31;
+  const int cc = lane % cpr, rw = lane / cpr;
+  const bool active = rw < RPW;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t h = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); h < p.bh; h += nw) {
+    float vv[VEC], acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = vv[e] = 0.f;
+    if (active) IO::unpack(__ldg(reinterpret_cast<const uint4 *>(p.v) + h * cpr + cc), vv);
+    const uint4 *Srow = reinterpret_cast<const uint4 *>(p.S) + (h * dk) * (int64_t)cpr + cc;
+    uint4 *Nrow = reinterpret_cast<uint4 *>(p.S_new) + (h * dk) * (int64_t)cpr + cc;
+    for (int i0 = rw; i0 < dk; i0 += RPW * RW) {
+      uint4 sv[RW];
+      float gv[RW], kv[RW], qv[RW];
+#pragma unroll
+      for (int u = 0; u < RW; ++u) {
+        const int i = i0 + u * RPW;
+        const bool ok = active && i < dk;
+        sv[u] = ok ? ldg_stream(Srow + (int64_t)i * cpr) : zero4();
+        gv[u] = ok ? IO::scalar(p.gk, h * dk + i) : 0.f;
+        kv[u] = ok ? IO::scalar(p.k, h * dk + i) : 0.f;
+        qv[u] = ok ? IO::scalar(p.q, h * dk + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < RW; ++u) {
+        const int i = i0 + u * RPW;
+        if (active && i < dk) {
+          float s[VEC], sn[VEC];
+          IO::unpack(sv[u], s);
+          const float di = expf(gv[u]);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            sn[e] = fmaf(di, s[e], kv[u] * vv[e]);
+            acc[e] = fmaf(qv[u], sn[e], acc[e]);
+          }
+          stg_stream(Nrow + (int64_t)i * cpr, IO::pack(sn));
+        }
+      }
+    }
+    float tot[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      tot[e] = 0.f;
+      for (int r = 0; r < RPW; ++r) tot[e] += __shfl_sync(0xffffffffu, acc[e], cc + r * cpr);
+      tot[e] *= p.scale;
+    }
+    if (rw == 0) stg_stream(reinterpret_cast<uint4 *>(p.o) + h * cpr + cc, IO::pack(tot));
   }
 }
 
@@ -185,9 +274,11 @@ bool overlap_bytes(const void *p, int64_t pb, const void *q, int64_t qb) {
 
 using namespace gemvk;
 
-extern "C" int gla_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
-                          void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, cudaStream_t stream) {
+extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const void *gk, const void *S,
+                             void *S_new, void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype,
+                             int variant, cudaStream_t stream) {
   if (dtype != GLA_F16 && dtype != GLA_BF16 && dtype != GLA_F32) return GEMV_ERR_DTYPE;
+  if (variant < GLA_VARIANT_AUTO || variant > GLA_VARIANT_WARP) return GEMV_ERR_CONFIG;
   if (bh < 0 || dk < 0 || dv < 0 || dk > kGlaMaxDk) return GEMV_ERR_ARG;
   if (bh == 0 || dv == 0) return GEMV_OK;
   const int es = dtype == GLA_F32 ? 4 : 2;
@@ -222,11 +313,41 @@ extern "C" int gla_decode(const void *q, const void *k, const void *v, const voi
   }
   if (major != 10 || minor != 3) return GEMV_ERR_DEVICE;
   const int cpr = (int)(dv / VEC);
-  const int RP = kGlaThreads / cpr;
-  const size_t smem = (size_t)(3 * dk + (int64_t)RP * dv) * sizeof(float);
+  // The CTA layout with several heads per round measured faster than a
+  // warp per head on every workload tried (4096 x 64 x 64 fp16: 18.5 vs
+  // 20.5 us; 16384 x 16 x 64 fp16: 20.5 vs 28.7 us; 4096 x 128 x 128 bf16:
+  // 48.5 vs 61.2 us), so it is the automatic choice.
+  if (variant == GLA_VARIANT_AUTO) variant = GLA_VARIANT_CTA;
+  if (variant == GLA_VARIANT_WARP && cpr > 32) return GEMV_ERR_CONFIG;
   GlaParams p;
   p.q = q; p.k = k; p.v = v; p.gk = gk; p.S = S; p.S_new = S_new; p.o = o;
-  p.bh = bh; p.dk = (int32_t)dk; p.dv = (int32_t)dv; p.scale = scale;
+  p.bh = bh; p.dk = (int32_t)dk; p.dv = (int32_t)dv; p.scale = scale; p.heads_per_cta = 1;
+  if (variant == GLA_VARIANT_WARP) {
+    void (*fw)(GlaParams) = dtype == GLA_F16 ? gla_decode_warp_kernel<F16>
+                            : dtype == GLA_BF16 ? gla_decode_warp_kernel<BF16> : gla_decode_warp_kernel<F32>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fw, kGlaThreads, 0) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      return GEMV_ERR_CONFIG;
+    }
+    const int64_t warps = kGlaThreads / 32;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (grid > (bh + warps - 1) / warps) grid = (bh + warps - 1) / warps;
+    fw<<<(unsigned)grid, kGlaThreads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return GEMV_ERR_CUDA;
+    return GEMV_OK;
+  }
+  // Heads side by side per CTA round: enough that each thread has about
+  // kGlaRowsInFlight rows of its head to stream (small heads), at least one
+  // row block of cpr threads per head.
+  int G = 1;
+  while (2 * G * cpr <= kGlaThreads && (int64_t)2 * G <= bh &&
+         (int64_t)dk * cpr * (2 * G) <= (int64_t)kGlaRowsInFlight * kGlaThreads)
+    G *= 2;
+  p.heads_per_cta = G;
+  const int RP = (kGlaThreads / G) / cpr;
+  const size_t smem = (size_t)(3 * (int64_t)G * dk + (int64_t)G * RP * dv) * sizeof(float);
   void (*fn)(GlaParams) = dtype == GLA_F16 ? gla_decode_kernel<F16>
                           : dtype == GLA_BF16 ? gla_decode_kernel<BF16> : gla_decode_kernel<F32>;
   if (smem > 48 * 1024) {
@@ -240,8 +361,14 @@ extern "C" int gla_decode(const void *q, const void *k, const void *v, const voi
     return GEMV_ERR_CONFIG;
   }
   int64_t grid = (int64_t)sms * per_sm;
-  if (grid > bh) grid = bh;
+  const int64_t rounds = (bh + G - 1) / G;
+  if (grid > rounds) grid = rounds;
   fn<<<(unsigned)grid, kGlaThreads, smem, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return GEMV_ERR_CUDA;
   return GEMV_OK;
+}
+
+extern "C" int gla_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
+                          void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, cudaStream_t stream) {
+  return gla_decode_ex(q, k, v, gk, S, S_new, o, bh, dk, dv, scale, dtype, GLA_VARIANT_AUTO, stream);
 }

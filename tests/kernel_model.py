@@ -350,30 +350,101 @@ def staged_shifted(a, j0, seglen, off, as_elems):
 
 
 
-def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=4):
-    """Index replay of ``gla_decode_kernel``: every state element of every head
-    is read and written exactly once by one thread, every partial slot and
-    every output element is in range."""
+def gla_heads_per_cta(bh, dk, cpr, threads=256, rows_in_flight=4):
+    """The host's choice of heads processed side by side per CTA round."""
+    G = 1
+    while 2 * G * cpr <= threads and 2 * G <= bh and dk * cpr * 2 * G <= rows_in_flight * threads:
+        G *= 2
+    return G
+
+
+def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=4, grid=None):
+    """Index replay of ``gla_decode_kernel`` (G heads per CTA round): every
+    state element of every head is read and written exactly once by one
+    thread, every staging, partial and output index is in range, and every
+    partial read by the o reduction was written in the same round."""
     vec = 16 // elem_bytes
     assert dv % vec == 0
     cpr = dv // vec
     assert 1 <= cpr <= threads
-    RP = threads // cpr
+    G = gla_heads_per_cta(bh, dk, cpr, threads, rows_in_flight)
+    assert G * cpr <= threads and threads % G == 0
+    TPG = threads // G
+    RP = TPG // cpr
+    assert RP >= 1
+    smem_floats = 3 * G * dk + G * RP * dv
+    rounds = -(-bh // G)
+    grid = rounds if grid is None else min(grid, rounds)
     touched = np.zeros((bh, dk, dv), dtype=np.int32)
-    smem_floats = 3 * dk + RP * dv
-    for h in range(bh):
-        for t in range(threads):
-            cc, rl = t % cpr, t // cpr
-            if rl >= RP:
-                continue
-            for i0 in range(rl, dk, RP * rows_in_flight):
-                for u in range(rows_in_flight):
-                    i = i0 + u * RP
-                    if i < dk:
-                        vidx = (h * dk + i) * cpr + cc  # 16-byte vector index of S / S_new
-                        assert 0 <= vidx < bh * dk * cpr
-                        touched[h, i, cc * vec:(cc + 1) * vec] += 1
-            assert 3 * dk + rl * dv + cc * vec + vec <= smem_floats
-            assert (h * dv) // vec + cc < bh * dv // vec
-    assert (touched == 1).all()
-    return {"smem_floats": smem_floats}
+    o_written = np.zeros((bh, dv), dtype=np.int32)
+    for blk in range(grid):
+        for r in range(blk, rounds, grid):
+            h0 = r * G
+            nh = min(G, bh - h0)
+            part_written = set()
+            for t in range(threads):
+                gi, tl = divmod(t, TPG)
+                cc, rl = tl % cpr, tl // cpr
+                if not (rl < RP and gi < nh):
+                    continue
+                h = h0 + gi
+                for i0 in range(rl, dk, RP * rows_in_flight):
+                    for u in range(rows_in_flight):
+                        i = i0 + u * RP
+                        if i < dk:
+                            vidx = (h * dk + i) * cpr + cc
+                            assert 0 <= vidx < bh * dk * cpr
+                            assert 2 * G * dk + gi * dk + i < 3 * G * dk  # qq[gi][i], the last staged array
+                            touched[h, i, cc * vec:(cc + 1) * vec] += 1
+                base = 3 * G * dk + (gi * RP + rl) * dv + cc * vec
+                assert base + vec <= smem_floats
+                part_written.update(range(base, base + vec))
+                assert (h * dv) // vec + cc < bh * dv // vec
+            for x in range(nh * dv):
+                g, j = divmod(x, dv)
+                for rb in range(RP):
+                    assert 3 * G * dk + (g * RP + rb) * dv + j in part_written
+                o_written[h0 + g, j] += 1
+    assert (touched == 1).all() and (o_written == 1).all()
+    return {"smem_floats": smem_floats, "heads_per_cta": G}
+
+
+def replay_gla_warp(bh, dk, dv, elem_bytes, warps_per_cta=8, grid=None, rows_in_flight=8):
+    """Index replay of ``gla_decode_warp_kernel``: warp w of the grid takes
+    heads w, w + warps, ...; lane l owns chunk l % cpr of rows l // cpr +
+    RPW * m.  Every state element of every head is read and written exactly
+    once, every shuffle source lane is a lane of the warp holding the same
+    chunk, and every o chunk is stored once."""
+    vec = 16 // elem_bytes
+    assert dv % vec == 0
+    cpr = dv // vec
+    assert 1 <= cpr <= 32
+    RPW = 32 // cpr
+    heads_per_grid = None
+    nwarps_total = -(-bh // warps_per_cta) * warps_per_cta
+    if grid is not None:
+        nwarps_total = min(grid, -(-bh // warps_per_cta)) * warps_per_cta
+    heads_per_grid = nwarps_total
+    touched = np.zeros((bh, dk, dv), dtype=np.int32)
+    o_written = np.zeros((bh, dv), dtype=np.int32)
+    for w in range(nwarps_total):
+        for h in range(w, bh, heads_per_grid):
+            for lane in range(32):
+                cc, rw = lane % cpr, lane // cpr
+                if rw < RPW:
+                    for i0 in range(rw, dk, RPW * rows_in_flight):
+                        for u in range(rows_in_flight):
+                            i = i0 + u * RPW
+                            if i < dk:
+                                vidx = (h * dk + i) * cpr + cc
+                                assert 0 <= vidx < bh * dk * cpr
+                                touched[h, i, cc * vec:(cc + 1) * vec] += 1
+                # the o reduction reads lanes cc + r * cpr, r < RPW: same chunk, every row group
+                srcs = [cc + r * cpr for r in range(RPW)]
+                assert all(0 <= x < 32 and x % cpr == cc for x in srcs)
+                assert sorted(x // cpr for x in srcs) == list(range(RPW))
+                if rw == 0:
+                    assert 0 <= h * cpr + cc < bh * cpr
+                    o_written[h, cc * vec:(cc + 1) * vec] += 1
+    assert (touched == 1).all() and (o_written == 1).all()
+    return {"warps": nwarps_total}

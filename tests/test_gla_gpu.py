@@ -69,29 +69,69 @@ def _check(q, k, v, gk, S_in, S_new, o, scale, label):
 SHAPES = [(64, 128, 128), (32, 64, 64), (8, 256, 128), (3, 17, 8), (2, 1, 512), (4, 100, 1024), (1, 4096, 64)]
 
 
-@pytest.mark.parametrize("bh,dk,dv", SHAPES)
+def _warp_ok(dv, dtype):
+    """One warp per head needs dv * element size <= 512 bytes."""
+    return dv * (4 if dtype == torch.float32 else 2) <= 512
+
+
+@pytest.mark.parametrize("bh,dk,dv", SHAPES + [(40, 64, 64), (9, 33, 256), (37, 16, 64), (11, 5, 24), (300, 8, 64)])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-def test_gla_parity(cuda_dev, bh, dk, dv, dtype):
+@pytest.mark.parametrize("variant", [g.GLA_VARIANT_AUTO, g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+def test_gla_parity(cuda_dev, bh, dk, dv, dtype, variant):
     if dtype == torch.float32 and dv // 4 > 256:
         pytest.skip("dv / 4 > 256 is outside the kernel's range for fp32")
+    if variant == g.GLA_VARIANT_WARP and not _warp_ok(dv, dtype):
+        with pytest.raises(g.GemvError) as ei:
+            q, k, v, gk, S = _make(bh, dk, dv, dtype, 1, cuda_dev)
+            g.gla_decode(q, k, v, gk, S, scale=1.0, variant=variant)
+        assert ei.value.status == g.GEMV_ERR_CONFIG
+        return
     q, k, v, gk, S = _make(bh, dk, dv, dtype, bh + dk + dv, cuda_dev)
     S_in = S.clone()
-    S_new, o = g.gla_decode(q, k, v, gk, S, scale=dk ** -0.5)
-    _check(q, k, v, gk, S_in, S_new, o, dk ** -0.5, f"{bh}x{dk}x{dv} {dtype}")
+    S_new, o = g.gla_decode(q, k, v, gk, S, scale=dk ** -0.5, variant=variant)
+    _check(q, k, v, gk, S_in, S_new, o, dk ** -0.5, f"{bh}x{dk}x{dv} {dtype} variant {variant}")
     assert torch.equal(S, S_in)  # out of place: S untouched
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-def test_gla_in_place(cuda_dev, dtype):
+@pytest.mark.parametrize("variant", [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+def test_gla_in_place(cuda_dev, dtype, variant):
     q, k, v, gk, S = _make(16, 128, 128, dtype, 5, cuda_dev)
     S_in = S.clone()
-    S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.125, S_new=S)
+    S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.125, S_new=S, variant=variant)
     assert S_new.data_ptr() == S.data_ptr()
-    _check(q, k, v, gk, S_in, S_new, o, 0.125, f"in place {dtype}")
+    _check(q, k, v, gk, S_in, S_new, o, 0.125, f"in place {dtype} variant {variant}")
+
+
+@pytest.mark.parametrize("bh,dk,dv,dtype", [(4096, 64, 64, torch.float16), (2600, 128, 128, torch.bfloat16),
+                                            (3000, 16, 128, torch.float32), (5, 200, 40, torch.float16)])
+def test_gla_layouts_agree(cuda_dev, bh, dk, dv, dtype):
+    """The two layouts store bit-identical states (same fmaf per element) and
+    o within the sum-order tolerance; the automatic choice is the CTA
+    layout."""
+    q, k, v, gk, S = _make(bh, dk, dv, dtype, 21, cuda_dev)
+    S_c, o_c = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_CTA)
+    S_w, o_w = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_WARP)
+    torch.cuda.synchronize()
+    assert torch.equal(_t(S_c), _t(S_w))
+    if bh <= 64:
+        _check(q, k, v, gk, S, S_w, o_w, 0.25, "warp layout")
+    else:
+        rows = torch.arange(0, bh, max(1, bh // 40), device=cuda_dev)
+        _check(q[rows], k[rows], v[rows], gk[rows], S[rows], S_w[rows], o_w[rows], 0.25, "warp layout sampled")
+        _check(q[rows], k[rows], v[rows], gk[rows], S[rows], S_c[rows], o_c[rows], 0.25, "cta layout sampled")
+    S_a, o_a = g.gla_decode(q, k, v, gk, S, scale=0.25)
+    torch.cuda.synchronize()
+    assert torch.equal(_t(o_a), _t(o_c)) and torch.equal(_t(S_a), _t(S_c))
+
+
+def _t(x):
+    return x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16)
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype):
+@pytest.mark.parametrize("variant", [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype, variant):
     """gk = 0 and small integers: every fp32 operation is exact, so the stored
     state and o equal the oracle rounded once."""
     gen = torch.Generator(device=cuda_dev)
@@ -100,7 +140,7 @@ def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype):
     ri = lambda *s: torch.randint(-3, 4, s, generator=gen, device=cuda_dev).to(dtype)
     q, k, v, S = ri(bh, dk), ri(bh, dk), ri(bh, dv), ri(bh, dk, dv)
     gk = torch.zeros((bh, dk), dtype=dtype, device=cuda_dev)
-    S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.5)
+    S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.5, variant=variant)
     torch.cuda.synchronize()
     fmt = FMT[dtype]
     ref_S, ref_o, _, _ = oracle.gla_ref_decode(_bits(q), _bits(k), _bits(v), _bits(gk), _bits(S), 0.5, fmt)
@@ -108,14 +148,15 @@ def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype):
     assert (_bits(o) == oracle.encode(ref_o, fmt)).all()
 
 
-def test_gla_multiple_steps_match_stepwise_oracle(cuda_dev):
+@pytest.mark.parametrize("variant", [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+def test_gla_multiple_steps_match_stepwise_oracle(cuda_dev, variant):
     """Ten chained decode steps on one state (in place), each checked."""
     bh, dk, dv = 12, 64, 64
     q, k, v, gk, S = _make(bh, dk, dv, torch.float32, 9, cuda_dev)
     for step in range(10):
         q, k, v, gk, _ = _make(bh, dk, dv, torch.float32, 100 + step, cuda_dev)
         S_prev = S.clone()
-        _, o = g.gla_decode(q, k, v, gk, S, scale=0.1, S_new=S)
+        _, o = g.gla_decode(q, k, v, gk, S, scale=0.1, S_new=S, variant=variant)
         _check(q, k, v, gk, S_prev, S, o, 0.1, f"step {step}")
 
 

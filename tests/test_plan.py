@@ -202,9 +202,19 @@ def test_tiles_index_replay_strided(gemv_lib, n, k, ldb, base_off, forced):
 
 
 @pytest.mark.parametrize("bh,dk,dv,es", [(3, 128, 128, 2), (2, 64, 64, 4), (5, 17, 8, 2), (1, 1, 2048, 2),
-                                         (2, 100, 1024, 4), (4, 256, 24, 2), (1, 0, 64, 2)])
-def test_gla_index_replay(bh, dk, dv, es):
-    kernel_model.replay_gla(bh, dk, dv, es)
+                                         (2, 100, 1024, 4), (4, 256, 24, 2), (1, 0, 64, 2), (7, 64, 64, 2),
+                                         (37, 16, 64, 2), (11, 5, 24, 2), (6, 3, 40, 4)])
+@pytest.mark.parametrize("grid", [1, 3, None])
+def test_gla_index_replay(bh, dk, dv, es, grid):
+    kernel_model.replay_gla(bh, dk, dv, es, grid=grid)
+
+
+def test_gla_heads_per_cta_choice():
+    """Small heads are processed several per CTA round (about 4 rows per
+    thread), large ones one per round."""
+    hp = kernel_model.gla_heads_per_cta
+    assert hp(4096, 64, 8) == 2 and hp(16384, 16, 8) == 8 and hp(2048, 128, 16) == 1
+    assert hp(1024, 256, 32) == 1 and hp(1, 16, 8) == 1 and hp(3, 16, 8) == 2
 
 
 # ------------------------------------------------------------- bulk variant --
@@ -308,3 +318,11 @@ def test_bulk_auto_plans_replay(gemv_lib, n, k, base_off):
     cfg = gemv_lib.gemv_plan(n, k, 0, base_off == 0, SM)
     assert cfg["variant"] == 4
     kernel_model.replay(n, k, cfg, base_off=base_off)
+
+
+@pytest.mark.parametrize("bh,dk,dv,es", [(3, 128, 128, 2), (2, 64, 64, 4), (5, 17, 8, 2), (9, 1, 256, 2),
+                                         (2, 100, 128, 4), (4, 256, 24, 2), (1, 0, 64, 2), (33, 64, 64, 2),
+                                         (17, 5, 48, 4)])
+@pytest.mark.parametrize("grid", [1, 2, None])
+def test_gla_warp_index_replay(bh, dk, dv, es, grid):
+    kernel_model.replay_gla_warp(bh, dk, dv, es, grid=grid)
