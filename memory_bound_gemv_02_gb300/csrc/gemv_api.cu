@@ -34,8 +34,7 @@ constexpr int kMaxGridSplit = 64;
 constexpr int kAutoVariant = GEMV_VARIANT_TILES;  // the planner's default family
 constexpr int kDefaultL2Prefetch = 0;              // tile rounds of L2 prefetch by default
 constexpr int kBulkDefaultStages = 2;              // ring buffers per warp of the bulk variant
-constexpr int64_t kBulkAutoBytes = 512LL << 20;    // B bytes from which the planner picks the bulk variant
-constexpr int64_t kBulkAutoBytesUnaligned = 192LL << 20;  // the same, rows not 16-byte aligned
+constexpr int64_t kBulkAutoBytes = 768LL << 20;    // B bytes from which the planner picks the bulk variant
 constexpr int kMaxSmemPerCta = 232448;  // 227 KiB, sm_100-family opt-in limit
 constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int64_t kSmemReservedPerCta = 1024;
@@ -45,6 +44,12 @@ constexpr int kProbeSinkWords = 16384;  // 64 KiB
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+inline int64_t pow2_ceil(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p *= 2;
+  return p;
+}
+
 inline int64_t pow2_floor(int64_t x) {
   int64_t p = 1;
   while (p * 2 <= x) p *= 2;
@@ -134,6 +139,21 @@ bool valid_tiles_RU(int R, int U) {
   return (R == 1 && (U == 8 || U == 4)) || (R == 2 && U == 4) || (R == 4 && U == 2);
 }
 
+// Warps per row (S) of the tiles kernel for rows of nt 16-byte blocks: the
+// smallest power-of-two split whose slices are at most 1024 blocks (16 KB
+// per warp and row; longer slices measured 4-10 % slower at k = 16384) and
+// that gives at least 80 % of the resident warps (sm x 32) a slice, without
+// cutting slices below 128 blocks.  Measured on GB300 against every (W, S,
+// R) over the workload shapes: this choice is the fastest or within 3 % of
+// it.
+int tiles_split(int64_t n, int64_t nt, int W, int sm) {
+  int S = (int)pow2_ceil(cdiv(nt, 1024));
+  if (S > W) S = W;
+  const int64_t fill = (int64_t)sm * 32 * 4 / 5;
+  while (2 * S <= W && n * S < fill && cdiv(nt, 2 * S) >= 128) S *= 2;
+  return S;
+}
+
 // Planner of the tiles variant (pure host arithmetic).
 //  * k-segments: as few as the shared-memory budget allows, more when the
 //    rows alone cannot give every SM work (split-K).
@@ -145,9 +165,13 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
                bool bulk = false) {
   const int NCLS = aligned ? 1 : 8;
   const int W_list[3] = {16, 8, 4};
+  // The tiles kernel runs 16-warp CTAs unless forced (measured best or
+  // within 3 % on every workload shape); the bulk kernel, whose shared
+  // memory limits it to one CTA per SM, tries smaller CTAs for small shapes.
+  const int nW = (bulk && !f->warps_per_cta) ? 3 : 1;
   gemv_config best{};
   bool have = false;
-  for (int wi = 0; wi < 3; ++wi) {
+  for (int wi = 0; wi < nW; ++wi) {
     const int W = f->warps_per_cta ? f->warps_per_cta : W_list[wi];
     if (!valid_W(W)) return GEMV_ERR_CONFIG;
     const int cps_warps = 32 / W;
@@ -163,11 +187,12 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     if (f->warp_split) {
       S = f->warp_split;
       if (S < 1 || S > W || W % S != 0) return GEMV_ERR_CONFIG;
+    } else if (!bulk) {
+      S = tiles_split(n, nt_est, W, sm);
     } else {
-      // Slices of about 32 * 16 blocks (16 loads per lane in two rounds):
-      // on GB300 this balanced per-warp depth against the cost of the
-      // per-tile slice reduction best (k = 4096 -> 1, 7168/8192 -> 2,
-      // 14336/16384 -> 4 warps per row).
+      // Bulk kernel: slices of about 32 * 16 blocks, so that each warp's
+      // ring streams several chunks per row (a whole row per warp measured
+      // up to 8 % slower at k = 7168).
       const int64_t q = (nt_est + 256) / 512;  // nt_est / 512, rounded
       S = (int)pow2_floor(q < 1 ? 1 : q);
       if (2 * S <= W && nt_est > 3 * S * 512 / 2) S *= 2;  // round up past 1.5x
@@ -192,21 +217,33 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
       U = f->unroll ? f->unroll : (R == 1 ? 8 : (R == 2 ? 4 : 2));
       if (!valid_tiles_RU(R, U)) return GEMV_ERR_CONFIG;
     } else {
-      const int64_t L = cdiv(nt_est, S);
-      if (S == 1 && L <= 64) {
-        R = 4; U = 2;
-      } else if (S == 1 && L <= 128) {
-        R = 2; U = 4;
-      } else if (L <= 128) {
-        R = 1; U = 4;
-      } else {
-        R = 1; U = 8;
+      R = 1;
+      U = cdiv(nt_est, S) <= 128 ? 4 : 8;
+      // Two rows per warp (four loads each, so a staged vector of a serves
+      // both) where every resident warp has two rows or more anyway and the
+      // last round of row tiles wastes no more warp slots than with one:
+      // 18432 x 7168 40.5 -> 38.6 us, 65536 x 4096 77.2 -> 76.4 us.
+      if (S == 1 && n >= 2LL * sm * 32) {
+        const int64_t nr = cdiv(n, NCLS);
+        auto round_fill = [&](int64_t RT) {
+          int64_t C = (int64_t)sm * cps_warps / Sg;
+          if (C > cdiv(nr, RT) * NCLS) C = cdiv(nr, RT) * NCLS;
+          C = C / NCLS * NCLS;
+          if (C < NCLS) C = NCLS;
+          const int64_t Cq = C / NCLS;
+          const int64_t rounds = cdiv(cdiv(nr, Cq), RT);
+          return ((double)nr / (double)Cq) / (double)(rounds * RT);
+        };
+        if (round_fill(2LL * W) >= 0.99 * round_fill(W)) {
+          R = 2;
+          U = 4;
+        }
       }
     }
     // row tiles and grid
-    const int64_t RT = (int64_t)(W / S) * R;
+    int64_t RT = (int64_t)(W / S) * R;
     const int64_t rows_per_class = cdiv(n, NCLS);
-    const int64_t groups = cdiv(rows_per_class, RT);  // tiles per class per segment
+    int64_t groups = cdiv(rows_per_class, RT);  // tiles per class per segment
     const int64_t as_elems = round_up(kseg + 24, 8);
     int NS = 0;  // bulk: ring buffers per warp
     if (bulk) {
@@ -240,6 +277,15 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
         Sg = Sg2;
         kseg = round_up(cdiv(k, Sg), 8);
         Sg = cdiv(k, kseg);
+        // The segments are shorter now: choose the tiles kernel's split for
+        // their length (few rows: R = 1 in any case).
+        if (!bulk && !f->warp_split && !f->rows_per_warp && !f->unroll) {
+          const int64_t nt2 = cdiv(kseg, 8) + (aligned ? 0 : 1);
+          S = tiles_split(n, nt2, W, sm);
+          U = cdiv(nt2, S) <= 128 ? 4 : 8;
+          RT = (int64_t)(W / S) * R;
+          groups = cdiv(rows_per_class, RT);
+        }
       }
     }
     int64_t C;
@@ -300,16 +346,17 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
                                                                             : kAutoVariant;
   const int variant = f->variant ? f->variant : auto_variant;
   if (variant == GEMV_VARIANT_TILES && f == &fz) {
-    // Nothing forced: the tiles plan, or the bulk variant with the same work
-    // split where it measured faster on GB300 (B of 512 MiB or more -- 192
-    // MiB or more when the rows are not 16-byte aligned -- streamed by at
-    // most 2 warps per row: 57344 x 7168 116.8 -> 114.5 us, 65536 x 7169
-    // 139.6 -> 134.5 us, 16384 x 7169 38.8 -> 37.7 us back to back).
+    // Nothing forced: the tiles plan, or the bulk variant where it measured
+    // faster on GB300 than the tiles plan: B of 768 MiB or more whose rows
+    // the tiles plan streams with one warp each (rows of at most 1024
+    // blocks; 57344 x 7168: 116.5 -> 114.5 us, 65536 x 7169: 135.3 -> 134.5
+    // us back to back).  Below that, and for longer rows, register
+    // streaming is as fast or faster.
     int st = plan_tiles(n, k, aligned, sm, f, out);
     const int64_t b_bytes = n * k * 2;
-    if (st == GEMV_OK && out->warp_split <= 2 && b_bytes >= (aligned ? kBulkAutoBytes : kBulkAutoBytesUnaligned)) {
+    if (st == GEMV_OK && out->warp_split == 1 && b_bytes >= kBulkAutoBytes) {
       gemv_config b{};
-      if (plan_tiles(n, k, aligned, sm, f, &b, true) == GEMV_OK && b.warp_split <= 2) *out = b;
+      if (plan_tiles(n, k, aligned, sm, f, &b, true) == GEMV_OK) *out = b;
     }
     return st;
   }
