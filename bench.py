@@ -521,7 +521,8 @@ def run_gla(args, dev):
 
 def run_case(args, dev):
     """Run one shape a few times and exit (for profiler captures):
-    --case N,K,DTYPE[,f32] [--calls C] [--config JSON]."""
+    --case N,K,DTYPE[,f32] [--calls C] [--config JSON] [--epilogue ACT]
+    (ACT: run gemv_fused with alpha 0.5, an fp32 bias and that activation)."""
     import torch
 
     import memory_bound_gemv_02_gb300 as g
@@ -532,10 +533,37 @@ def run_case(args, dev):
     B, a = inputs.make_inputs(n, k, dtype, "normal", 0, dev)
     c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
     cfg = json.loads(args.config) if args.config else None
+    bias = torch.linspace(-1, 1, n, device=dev) if args.epilogue else None
     for _ in range(args.calls):
-        g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=cfg)
+        if args.epilogue:
+            g.gemv_fused(B, a, c=c, out_fp32=out_fp32, alpha=0.5, beta=1.0, bias=bias, activation=args.epilogue,
+                         config=cfg)
+        else:
+            g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=cfg)
     torch.cuda.synchronize()
-    print(json.dumps({"case": args.case, "calls": args.calls, "config": g.gemv_last_config()}))
+    print(json.dumps({"case": args.case, "calls": args.calls, "epilogue": args.epilogue,
+                      "config": g.gemv_last_config()}))
+    return 0
+
+
+def run_gla_case(args, dev):
+    """One GLA decode workload a few times, in place (for profiler captures):
+    --gla-case BH,DK,DV,DTYPE [--calls C] [--gla-variant V]."""
+    import torch
+
+    import memory_bound_gemv_02_gb300 as g
+    bh, dk, dv = (int(x) for x in args.gla_case.split(",")[:3])
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[args.gla_case.split(",")[3]]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    q, k, v = ((torch.rand((bh, x), generator=gen, device=dev) * 2 - 1).to(dt) for x in (dk, dk, dv))
+    gk = (-3 * torch.rand((bh, dk), generator=gen, device=dev)).to(dt)
+    S = torch.randn((bh, dk, dv), generator=gen, device=dev).to(dt)
+    o = torch.empty((bh, dv), dtype=dt, device=dev)
+    for _ in range(args.calls):
+        g.gla_decode(q, k, v, gk, S, scale=dk ** -0.5, S_new=S, o=o, variant=args.gla_variant)
+    torch.cuda.synchronize()
+    print(json.dumps({"gla_case": args.gla_case, "calls": args.calls, "variant": args.gla_variant}))
     return 0
 
 
@@ -555,6 +583,8 @@ def run_ours(args, world, rank, local):
         return run_sweep(args, dev)
     if args.case:
         return run_case(args, dev)
+    if args.gla_case:
+        return run_gla_case(args, dev)
     if args.gla:
         return run_gla(args, dev)
 
@@ -707,6 +737,10 @@ def main(argv=None):
     ap.add_argument("--gla", action="store_true", help="time the GLA decode step workloads instead")
     ap.add_argument("--gla-steps", type=int, default=300)
     ap.add_argument("--config", default=None, help="JSON launch configuration forced with --case")
+    ap.add_argument("--epilogue", default=None, choices=["none", "relu", "sigmoid", "silu"],
+                    help="with --case: run the fused-epilogue entry point with this activation and a bias")
+    ap.add_argument("--gla-case", default=None, help="BH,DK,DV,DTYPE: run that GLA decode step --calls times")
+    ap.add_argument("--gla-variant", type=int, default=0, help="GLA kernel layout forced with --gla-case")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

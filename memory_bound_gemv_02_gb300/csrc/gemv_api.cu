@@ -146,11 +146,27 @@ bool valid_tiles_RU(int R, int U) {
 // cutting slices below 128 blocks.  Measured on GB300 against every (W, S,
 // R) over the workload shapes: this choice is the fastest or within 3 % of
 // it.
-int tiles_split(int64_t n, int64_t nt, int W, int sm) {
+//
+// With split-K (Sg k-segments) every segment of a row is a unit of its own,
+// so the fill counts n * S * Sg.  Few rows per CTA can leave most warps of
+// the last round of row tiles idle: while a round is less than 75 % full, S
+// keeps doubling as long as that fills the rounds better (300 x 100003: 4
+// warps per row 21.0 us, 16 warps per row 18.8 us).
+int tiles_split(int64_t n, int64_t nt, int W, int sm, int64_t Sg, int NCLS, int cps_warps) {
   int S = (int)pow2_ceil(cdiv(nt, 1024));
   if (S > W) S = W;
   const int64_t fill = (int64_t)sm * 32 * 4 / 5;
-  while (2 * S <= W && n * S < fill && cdiv(nt, 2 * S) >= 128) S *= 2;
+  while (2 * S <= W && n * S * Sg < fill && cdiv(nt, 2 * S) >= 128) S *= 2;
+  auto round_fill = [&](int s) {
+    const int64_t RT = W / s, nr = cdiv(n, NCLS);
+    int64_t C = (int64_t)sm * cps_warps / Sg;
+    if (C > cdiv(nr, RT) * NCLS) C = cdiv(nr, RT) * NCLS;
+    C = C / NCLS * NCLS;
+    if (C < NCLS) C = NCLS;
+    const int64_t Cq = C / NCLS;
+    return ((double)nr / (double)Cq) / (double)(cdiv(cdiv(nr, Cq), RT) * RT);
+  };
+  while (2 * S <= W && cdiv(nt, 2 * S) >= 128 && round_fill(S) < 0.75 && round_fill(2 * S) > round_fill(S)) S *= 2;
   return S;
 }
 
@@ -188,7 +204,7 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
       S = f->warp_split;
       if (S < 1 || S > W || W % S != 0) return GEMV_ERR_CONFIG;
     } else if (!bulk) {
-      S = tiles_split(n, nt_est, W, sm);
+      S = tiles_split(n, nt_est, W, sm, Sg, NCLS, cps_warps);
     } else {
       // Bulk kernel: slices of about 32 * 16 blocks, so that each warp's
       // ring streams several chunks per row (a whole row per warp measured
@@ -281,7 +297,7 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
         // their length (few rows: R = 1 in any case).
         if (!bulk && !f->warp_split && !f->rows_per_warp && !f->unroll) {
           const int64_t nt2 = cdiv(kseg, 8) + (aligned ? 0 : 1);
-          S = tiles_split(n, nt2, W, sm);
+          S = tiles_split(n, nt2, W, sm, Sg, NCLS, cps_warps);
           U = cdiv(nt2, S) <= 128 ? 4 : 8;
           RT = (int64_t)(W / S) * R;
           groups = cdiv(rows_per_class, RT);
