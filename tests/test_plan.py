@@ -338,3 +338,15 @@ def test_bulk_auto_plans_replay(gemv_lib, n, k, base_off):
 @pytest.mark.parametrize("grid", [1, 2, None])
 def test_gla_warp_index_replay(bh, dk, dv, es, grid):
     kernel_model.replay_gla_warp(bh, dk, dv, es, grid=grid)
+
+
+@pytest.mark.parametrize("n,k,base_off,R", [(18433, 1003, 3, 2), (19456, 512, 0, 2), (10007, 1003, 3, 1),
+                                             (300, 100003, 5, 1), (12000, 2056, 0, 1)])
+def test_default_plan_replay_two_rows_and_split_k(gemv_lib, n, k, base_off, R):
+    """Default plans of the regimes the planner tuning introduced -- two rows
+    per warp for many rows (aligned and unaligned; one row where two would
+    leave more of the last round idle), split-K with 16 warps per row for
+    few unaligned rows -- replayed in full."""
+    cfg = gemv_lib.gemv_plan(n, k, 0, base_off == 0, SM)
+    assert cfg["rows_per_warp"] == R
+    kernel_model.replay(n, k, cfg, base_off=base_off)
