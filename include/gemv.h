@@ -91,7 +91,8 @@ enum {
                                  kernel's completion (and its memory) before reading or
                                  writing any global memory */
   GEMV_OVERLAP_PDL_PREFETCH_B = 2, /* as GEMV_OVERLAP_PDL, and each CTA streams its first tile
-                                 of B into registers before waiting.  The caller guarantees
+                                 of B into registers (bulk variant: its first ring buffers
+                                 into shared memory) before waiting.  The caller guarantees
                                  that no work still running on the stream writes B (true
                                  for weights); a and c are still accessed only after the
                                  wait */
@@ -111,6 +112,7 @@ enum {
  *                 the general variant).  The a-vector chunk read from shared
  *                 memory is reused across the R rows.  Tiles variant:
  *                 (R, unroll) is one of (1, 8), (1, 4), (2, 4), (4, 2).
+ *                 Bulk variant: 1.
  *  warps_per_cta  W: 4, 8 or 16 warps per CTA.
  *  warp_split     Sw: warps of one CTA that share a row, each streaming a
  *                 contiguous slice of it; their partial sums are combined
@@ -122,7 +124,8 @@ enum {
  *                 variant: row_blocks is the CTA count per k-segment, a
  *                 multiple of 8 unless k % 8 == 0 and B is 16-byte aligned.
  *  smem_bytes     dynamic shared memory per CTA (the staged a segment plus
- *                 the cross-warp partials).
+ *                 the cross-warp partials; bulk variant: plus the warps'
+ *                 ring buffers and their mbarriers).
  *  launches       kernels per call: 1, or 2 with split-K.
  *  k_segment      columns per k-segment (a multiple of 8 except when Sg == 1).
  *  row_blocks     number of row blocks (ctas / grid_split).

@@ -170,13 +170,15 @@ int tiles_split(int64_t n, int64_t nt, int W, int sm, int64_t Sg, int NCLS, int 
   return S;
 }
 
-// Planner of the tiles variant (pure host arithmetic).
+// Planner of the tiles and bulk variants (pure host arithmetic).
 //  * k-segments: as few as the shared-memory budget allows, more when the
 //    rows alone cannot give every SM work (split-K).
-//  * S (warps per row) so that a slice is at most 32*8 16-byte blocks, i.e.
-//    at most 8 loads per lane; short rows are instead streamed R at a time.
-//  * C (CTAs per segment): every SM busy at 32 resident warps, a multiple
-//    of 8 (one row class per CTA) unless the rows are 16-byte aligned.
+//  * S (warps per row): tiles_split() for the tiles kernel; slices of about
+//    512 blocks for the bulk kernel.  Tiles kernel: R = 2 rows per warp
+//    side by side where every resident warp has two rows anyway.
+//  * C (CTAs per segment): every SM busy at 32 resident warps (fewer when
+//    shared memory limits the CTAs per SM), a multiple of 8 (one row class
+//    per CTA) unless the rows are 16-byte aligned.
 int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f, gemv_config *out,
                bool bulk = false) {
   const int NCLS = aligned ? 1 : 8;
@@ -206,9 +208,9 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     } else if (!bulk) {
       S = tiles_split(n, nt_est, W, sm, Sg, NCLS, cps_warps);
     } else {
-      // Bulk kernel: slices of about 32 * 16 blocks, so that each warp's
-      // ring streams several chunks per row (a whole row per warp measured
-      // up to 8 % slower at k = 7168).
+      // Bulk kernel: slices of about 512 blocks (two 4 KB ring chunks), so
+      // that each warp's ring streams several chunks per row (a whole row
+      // per warp measured up to 8 % slower at k = 7168).
       const int64_t q = (nt_est + 256) / 512;  // nt_est / 512, rounded
       S = (int)pow2_floor(q < 1 ? 1 : q);
       if (2 * S <= W && nt_est > 3 * S * 512 / 2) S *= 2;  // round up past 1.5x
