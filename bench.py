@@ -390,6 +390,19 @@ def host_overhead_us(L, n, k, dt, dev, stream):
     return statistics.median(per) * 1e6
 
 
+def native_host_overhead():
+    """Host microseconds per cached gemv() call and per empty-kernel launch,
+    measured by the library's native tool (C++, steady_clock, 10^4 calls);
+    None if the tool is not built."""
+    from memory_bound_gemv_02_gb300 import _build
+    if not os.path.exists(_build.HOST_TOOL):
+        return None
+    r = subprocess.run([_build.HOST_TOOL], capture_output=True, text=True, timeout=120)
+    if r.returncode != 0:
+        raise RuntimeError(f"host-overhead tool failed: {r.stdout} {r.stderr}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, variant=0):
     """One shape: µs per call three ways -- isolated (CUDA events around each
     launch), back to back, and back to back with programmatic dependent
@@ -428,12 +441,32 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, var
     return {"n": n, "k": k, "dtype": dtype, "out": "f32" if out_fp32 else dtype, "dist": dist,
             "bytes": nbytes, "b_copies": copies,
             "us_isolated_median": round(iso, 3), "us_isolated_min": round(min(per) * 1e3, 3),
+            "us_isolated_p90": round(sorted(per)[int(0.9 * (len(per) - 1))] * 1e3, 3),
             "stddev_over_median": round(statistics.pstdev(per) / statistics.median(per), 4),
             "us_back_to_back": round(b2b, 3), "us_back_to_back_pdl": round(b2b_pdl, 3),
             "gbs_isolated": round(nbytes / iso / 1e3, 1), "gbs_back_to_back": round(nbytes / b2b / 1e3, 1),
             "gbs_back_to_back_pdl": round(nbytes / b2b_pdl / 1e3, 1),
             "config": {kk: cfg[kk] for kk in ("variant", "rows_per_warp", "unroll", "warps_per_cta",
                                               "warp_split", "grid_split", "ctas", "stages")}}
+
+
+def torch_mv_us(n, k, dtype, out_fp32, dist, dev, steps):
+    """torch.mv on the same shape (back to back over copies of B larger than
+    L2; output in the input type), for context."""
+    import torch
+
+    from memory_bound_gemv_02_gb300 import inputs
+    B, a = inputs.make_inputs(n, k, dtype, dist, 0, dev)
+    copies = max(2, min(16, -(-3 * L2_BYTES // max(1, n * k * 2))))
+    Bs = [B] + [B.clone() for _ in range(copies - 1)]
+    outs = [torch.empty(n, dtype=B.dtype, device=dev) for _ in Bs]
+    def mv(Bx, o):
+        torch.mv(Bx, a, out=o)
+        return 0
+
+    el = time_batch([(mv, (Bx, o)) for Bx, o in zip(Bs, outs)], steps, 10)
+    del Bs, outs
+    return el / steps * 1e6
 
 
 def run_sweep(args, dev):
@@ -452,6 +485,8 @@ def run_sweep(args, dev):
                          variant=g.GEMV_VARIANT_BULK)
         r["bulk"] = {kk: rb[kk] for kk in ("us_isolated_median", "us_back_to_back", "us_back_to_back_pdl",
                                            "gbs_back_to_back_pdl", "config")}
+        # context only (never a target): torch.mv (cuBLAS) on the same shape and box
+        r["torch_mv_us_back_to_back"] = round(torch_mv_us(n, k, dtype, out_fp32, dist, dev, args.sweep_steps), 3)
         out.write(json.dumps(r) + "\n")
         out.flush()
         print(json.dumps(r), file=sys.stderr, flush=True)
@@ -685,6 +720,7 @@ def run_ours(args, world, rank, local):
     probe_gbs = n * k * 2 / (statistics.median(pper) / 1e3) / 1e9
 
     host_us = host_overhead_us(L, 256, 512, 0, dev, s)
+    native = native_host_overhead()
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -710,6 +746,8 @@ def run_ours(args, world, rank, local):
                      "traffic": profiled_traffic("7168x16384_f16", cfg)},
         "probe_read_gbs": round(probe_gbs, 1),
         "host_us_per_call": round(host_us, 3),
+        "host_us_per_call_native": None if native is None else native["gemv_us"],
+        "empty_launch_us_native": None if native is None else native["empty_launch_us"],
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": n * k * 2 + k * 2, "d2h_bytes_per_step": n * out_bytes},
         "gpu_launches": args.steps * int(cfg["launches"]),

@@ -20,6 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build", "gemv")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgemv.so")
+HOST_TOOL_SRC = "host_overhead_main.cu"
+HOST_TOOL = os.path.join(LIBDIR, "gemv_host_overhead")  # native host-overhead measurement
 
 SOURCES = ["gemv_api.cu", "gemv_kernels_f16.cu", "gemv_kernels_bf16.cu", "gemv_bulk_f16.cu", "gemv_bulk_bf16.cu",
            "gemv_probe.cu", "gla_decode.cu"]
@@ -42,10 +44,10 @@ def nvcc() -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(HOST_TOOL):
         return True
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [os.path.abspath(__file__)]
+    t = min(os.path.getmtime(LIB), os.path.getmtime(HOST_TOOL))
+    deps = [os.path.join(CSRC, s) for s in SOURCES + [HOST_TOOL_SRC]] + HEADERS + [os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
@@ -76,6 +78,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+        # the native host-overhead tool, linked against the library just built
+        tmp = HOST_TOOL + f".tmp{os.getpid()}"
+        cmd = [exe, *NVCC_FLAGS, *extra_flags, os.path.join(CSRC, HOST_TOOL_SRC), "-o", tmp,
+               "-L" + LIBDIR, "-lgemv", "-Xlinker", "-rpath,$ORIGIN"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"host-overhead tool build failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, HOST_TOOL)
         return LIB
 
 

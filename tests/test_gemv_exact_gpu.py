@@ -10,6 +10,7 @@ variant, split or alignment.  That pins tails, split-K and the general
 from __future__ import annotations
 
 import itertools
+import os
 import time
 
 import numpy as np
@@ -354,3 +355,18 @@ def test_overlap_prefetch_ba_shared_input(cuda_dev, variant):
     for i, B in enumerate(Bs):
         check_against_oracle(outs[i], B, a, False, label=f"shared input, B{i}")
     check_against_oracle(c, Bs[-1], a, False, label="last writer of c")
+
+
+def test_native_host_overhead_tool(cuda_dev):
+    """The native (C++) measurement of the host cost of a cached gemv() call:
+    under 10 us, and within a few microseconds of an empty kernel launch."""
+    import json
+    import subprocess
+
+    from memory_bound_gemv_02_gb300 import _build
+    assert os.path.exists(_build.HOST_TOOL), "the build makes the native host-overhead tool"
+    r = subprocess.run([_build.HOST_TOOL], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert 0 < d["gemv_us"] < 10.0
+    assert 0 < d["empty_launch_us"] <= d["gemv_us"] + 1.0
