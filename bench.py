@@ -419,15 +419,12 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, var
     c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
     dt = g.dtype_code(B.dtype, out_fp32)
     s = torch.cuda.current_stream().cuda_stream
-    fc = g.GemvConfig()
+    fc = g.GemvConfig()  # overlap 0: plain launches
     fc.variant = variant
     g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=fc)
     cfg = g.gemv_last_config()
-    if variant:
-        plain = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(fc), s))
-                 for Bx in Bs]
-    else:
-        plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in Bs]
+    plain = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(fc), s))
+             for Bx in Bs]
     ov = g.GemvConfig()
     ov.variant = variant
     ov.overlap = g.GEMV_OVERLAP_PDL_PREFETCH_B
@@ -677,10 +674,15 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak()
 
     # Context (untimed for `value`): the same calls without overlap, back to
-    # back, and one at a time with CUDA events around each launch.
-    plain = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in (B, B2)]
+    # back, and one at a time with CUDA events around each launch; and plain
+    # gemv() calls (programmatic dependent launch without the B prefetch).
+    none_cfg = g.GemvConfig()  # overlap 0
+    plain = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(none_cfg), s))
+             for Bx in (B, B2)]
     nplain = min(args.steps, 2000)
     us_plain = time_batch(plain, nplain, 10) / nplain * 1e6
+    default = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in (B, B2)]
+    us_default = time_batch(default, nplain, 10) / nplain * 1e6
     # Calls that share their input vector (both B and a unwritten by the
     # work in flight, e.g. the projections of one activation) may also stage
     # a before the wait.
@@ -738,6 +740,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_call": round(mean_launch_ms * 1e3, 3),
         "us_per_call_no_overlap": round(us_plain, 3),
+        "us_per_call_gemv_default": round(us_default, 3),
         "us_per_call_shared_input": round(us_shared, 3),
         "us_per_call_isolated_median": round(us_iso, 3),
         "pct_of_nominal_8tbps": round(100 * achieved / NOMINAL_HBM_GBS, 1),

@@ -86,7 +86,8 @@ enum {
 /* Launch overlap with the preceding work on the stream (gemv_config.overlap). */
 enum {
   GEMV_OVERLAP_NONE = 0,      /* ordinary stream-ordered launch */
-  GEMV_OVERLAP_PDL = 1,       /* programmatic dependent launch: the kernel may be scheduled
+  GEMV_OVERLAP_PDL = 1,       /* (what gemv(), gemv_host() and calls without a configuration
+                                 use) programmatic dependent launch: the kernel may be scheduled
                                  while the preceding kernel drains; it waits for that
                                  kernel's completion (and its memory) before reading or
                                  writing any global memory */
@@ -172,6 +173,11 @@ typedef struct gemv_config {
  *         returns GEMV_OK.  k == 0 sets c to +0 (the empty sum).
  *  dtype  GEMV_F16, GEMV_BF16, GEMV_F16_OUT_F32 or GEMV_BF16_OUT_F32.
  *
+ * The kernel is launched as a programmatic dependent launch
+ * (GEMV_OVERLAP_PDL): it may be scheduled while the preceding kernel on the
+ * stream drains, but reads and writes no memory before that kernel has
+ * completed, so ordering is that of a plain launch.
+ *
  * The first call for a (device, n, k, dtype, alignment) key builds and caches
  * the launch configuration; later calls are a lookup plus one launch (two
  * with split-K).  A split-K configuration uses a library-owned fp32
@@ -185,7 +191,8 @@ int gemv(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
 
 /*
  * As gemv(), with a configuration forced field by field (zero fields left
- * to the planner).  `forced` may be NULL (same as gemv()).  An impossible
+ * to the planner; `overlap` is taken as given, so 0 is a plain launch).
+ * `forced` may be NULL (same as gemv()).  An impossible
  * configuration (e.g. the aligned variant for k % 8 != 0, W not in
  * {4, 8, 16}, Sw not dividing W) returns GEMV_ERR_CONFIG.  Forced
  * configurations are not cached.  For tests and benchmarks.

@@ -326,6 +326,9 @@ def test_overlap_uses_cached_plan(cuda_dev):
     B, a = inputs.make_inputs(777, 5000, "bf16", "uniform", 7, cuda_dev)
     g.gemv(B, a)
     base = g.gemv_last_config()
+    assert base["overlap"] == g.GEMV_OVERLAP_PDL  # gemv() launches as a programmatic dependent launch
+    g.gemv_ex(B, a, config={})
+    assert g.gemv_last_config()["overlap"] == g.GEMV_OVERLAP_NONE  # a given configuration is taken as is
     g.gemv_ex(B, a, config={"overlap": 2})
     got = g.gemv_last_config()
     assert got["overlap"] == 2
