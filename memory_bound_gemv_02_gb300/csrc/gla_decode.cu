@@ -126,6 +126,10 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_kernel(GlaParams p) {
   float *part = qq + G * dk;              // row-block partials of o [G][RP][dv]
   const int t = threadIdx.x;
   const int gi = t / TPG, tl = t % TPG;   // head slot of this thread, its index in the slot
+  // Launched as a programmatic dependent launch: let the next kernel be
+  // scheduled early, and touch no memory before the previous one is done.
+  allow_dependents();
+  wait_for_predecessor();
   const int cc = tl % cpr, rl = tl / cpr;
   const int64_t rounds = (p.bh + G - 1) / G;
 
@@ -217,6 +221,8 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_warp_kernel(GlaParams 
   const int cc = lane % cpr, rw = lane / cpr;
   const bool active = rw < RPW;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  allow_dependents();
+  wait_for_predecessor();
   for (int64_t h = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); h < p.bh; h += nw) {
     float vv[VEC], acc[VEC];
 #pragma unroll
@@ -261,6 +267,26 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_warp_kernel(GlaParams 
     }
     if (rw == 0) stg_stream(reinterpret_cast<uint4 *>(p.o) + h * cpr + cc, IO::pack(tot));
   }
+}
+
+// Launch a GLA kernel as a programmatic dependent launch (the kernels wait
+// for the preceding kernel before touching memory, so this orders like a
+// plain launch and only lets the launch overlap the predecessor's drain).
+cudaError_t pdl_launch(const void *fn, unsigned grid, size_t smem, cudaStream_t stream, GlaParams p) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kGlaThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  void *args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&lc, fn, args);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 bool overlap_bytes(const void *p, int64_t pb, const void *q, int64_t qb) {
@@ -334,8 +360,7 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
     const int64_t warps = kGlaThreads / 32;
     int64_t grid = (int64_t)sms * per_sm;
     if (grid > (bh + warps - 1) / warps) grid = (bh + warps - 1) / warps;
-    fw<<<(unsigned)grid, kGlaThreads, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return GEMV_ERR_CUDA;
+    if (pdl_launch((const void *)fw, (unsigned)grid, 0, stream, p) != cudaSuccess) return GEMV_ERR_CUDA;
     return GEMV_OK;
   }
   // Heads side by side per CTA round: enough that each thread has about
@@ -363,8 +388,7 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
   int64_t grid = (int64_t)sms * per_sm;
   const int64_t rounds = (bh + G - 1) / G;
   if (grid > rounds) grid = rounds;
-  fn<<<(unsigned)grid, kGlaThreads, smem, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return GEMV_ERR_CUDA;
+  if (pdl_launch((const void *)fn, (unsigned)grid, smem, stream, p) != cudaSuccess) return GEMV_ERR_CUDA;
   return GEMV_OK;
 }
 
