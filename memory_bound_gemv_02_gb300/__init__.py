@@ -181,7 +181,9 @@ def _operands(B: torch.Tensor, a: torch.Tensor, c, out_fp32: bool):
 def gemv(B: torch.Tensor, a: torch.Tensor, c: torch.Tensor | None = None, out_fp32: bool = False,
          stream=None) -> torch.Tensor:
     """c = B @ a on B's device, asynchronously on ``stream`` (default: the
-    current torch stream).  Returns c (allocated if not given)."""
+    current torch stream), launched as a programmatic dependent launch that
+    touches no memory before the preceding kernel has completed.  Returns c
+    (allocated if not given)."""
     n, k, c = _operands(B, a, c, out_fp32)
     with torch.cuda.device(B.device):
         st = lib().gemv(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
@@ -192,7 +194,8 @@ def gemv(B: torch.Tensor, a: torch.Tensor, c: torch.Tensor | None = None, out_fp
 
 def gemv_ex(B, a, c=None, out_fp32: bool = False, config=None, stream=None) -> torch.Tensor:
     """``gemv`` with a forced launch configuration (dict or GemvConfig;
-    zero/missing fields are left to the planner)."""
+    zero/missing fields are left to the planner, except ``overlap``, which
+    is taken as given: 0 is a plain launch).  ``config=None`` is ``gemv``."""
     n, k, c = _operands(B, a, c, out_fp32)
     with torch.cuda.device(B.device):
         st = lib().gemv_ex(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
