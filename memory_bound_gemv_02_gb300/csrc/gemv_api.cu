@@ -30,7 +30,8 @@ namespace gemvk {
 namespace {
 
 constexpr int64_t kMaxSegment = 32768;  // columns of a staged per CTA (64 KiB of shared memory)
-constexpr int kMaxGridSplit = 64;
+constexpr int kMaxGridSplit = 64;              // most k-segments the planner adds to fill the GPU
+constexpr int64_t kMaxSegments = 65536;         // most k-segments of any plan: k <= INT32_MAX in 32768-column segments
 constexpr int kAutoVariant = GEMV_VARIANT_TILES;  // the planner's default family
 constexpr int kDefaultL2Prefetch = 0;              // tile rounds of L2 prefetch by default
 constexpr int kBulkDefaultStages = 2;              // ring buffers per warp of the bulk variant
@@ -43,6 +44,15 @@ constexpr int kReduceThreads = 256;
 constexpr int kProbeSinkWords = 16384;  // 64 KiB
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Blocks of the split-K second pass: a thread per row for up to 32
+// segments, a warp per row beyond (the kernel's two modes); grid-stride
+// loops cover any remainder past the 65535-block cap.
+inline unsigned reduce_blocks(int64_t n, int64_t sg) {
+  int64_t b = cdiv(n, sg > 32 ? kReduceThreads / 32 : kReduceThreads);
+  if (b > 65535) b = 65535;
+  return (unsigned)(b < 1 ? 1 : b);
+}
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 inline int64_t pow2_ceil(int64_t x) {
   int64_t p = 1;
@@ -195,7 +205,7 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
     const int cps_warps = 32 / W;
     // k-segments
     int64_t Sg = f->grid_split ? f->grid_split : cdiv(k, kMaxSegment);
-    if (Sg < 1 || Sg > kMaxGridSplit) return GEMV_ERR_CONFIG;
+    if (Sg < 1 || Sg > kMaxSegments) return GEMV_ERR_CONFIG;
     int64_t kseg = (Sg == 1) ? k : round_up(cdiv(k, Sg), 8);
     Sg = cdiv(k, kseg);
     if (kseg > kMaxSegment) return GEMV_ERR_CONFIG;
@@ -424,12 +434,11 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
     int64_t Sg;
     if (f->grid_split) {
       Sg = f->grid_split;
-      if (Sg < 1 || Sg > kMaxGridSplit) return GEMV_ERR_CONFIG;
+      if (Sg < 1 || Sg > kMaxSegments) return GEMV_ERR_CONFIG;
     } else {
       Sg = cdiv(k, kMaxSegment);
       const int64_t need = split > Sw ? cdiv(split, Sw) : 1;
-      if (need > Sg) Sg = need;
-      if (Sg > kMaxGridSplit) Sg = kMaxGridSplit;
+      if (need > Sg) Sg = need > kMaxGridSplit ? (Sg > kMaxGridSplit ? Sg : kMaxGridSplit) : need;
       // a forced CTA count caps the split (but not below what k requires)
       if (f->ctas && Sg > f->ctas) Sg = f->ctas > cdiv(k, kMaxSegment) ? f->ctas : cdiv(k, kMaxSegment);
     }
@@ -616,9 +625,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
       e = cudaMemsetAsync(c, 0, (size_t)n * out_elem_bytes(dtype), stream);
     } else {
       ReduceKernel rk = lookup_reduce(dtype);
-      int64_t blocks = cdiv(n, kReduceThreads);
-      if (blocks > 65535) blocks = 65535;
-      rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(nullptr, c, n, 0, ep);
+      rk<<<reduce_blocks(n, 0), kReduceThreads, 0, stream>>>(nullptr, c, n, 0, ep);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return cuda_fail(e);
@@ -713,9 +720,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   if (e != cudaSuccess) return cuda_fail(e);
   if (cfg.grid_split > 1) {
     ReduceKernel rk = lookup_reduce(dtype);
-    int64_t blocks = cdiv(n, kReduceThreads);
-    if (blocks > 65535) blocks = 65535;
-    lc.gridDim = dim3((unsigned)blocks);
+    lc.gridDim = dim3(reduce_blocks(n, cfg.grid_split));
     lc.blockDim = dim3(kReduceThreads);
     lc.dynamicSmemBytes = 0;
     const float *wsc = ws;
@@ -1039,9 +1044,8 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
   if (e != cudaSuccess) return cuda_fail(e);
   if (cfg.grid_split > 1) {
     ReduceKernel rk = lookup_reduce(dtype);
-    int64_t blocks = cdiv(n, kReduceThreads);
-    if (blocks > 65535) blocks = 65535;
-    rk<<<(unsigned)blocks, kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split, identity_epilogue());
+    rk<<<reduce_blocks(n, cfg.grid_split), kReduceThreads, 0, stream>>>(ws, c, n, cfg.grid_split,
+                                                                           identity_epilogue());
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
   }

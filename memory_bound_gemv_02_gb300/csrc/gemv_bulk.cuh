@@ -114,6 +114,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_bulk_kernel(const Params 
   const int t1 = t0 + L < nt ? t0 + L : nt;
   const int64_t nloc = nr > cq ? (nr - cq + Cq - 1) / Cq : 0;
   const int64_t ngroups = (nloc + RT - 1) / RT;
+  if (ngroups == 0) {  // no rows for this CTA (a short row class): no staging, no loads
+    allow_dependents();
+    return;
+  }
   auto row_of = [&](int64_t m) -> int64_t { return NCLS * (cq + (int64_t)Cq * m) + cls; };
   auto block_of = [&](int64_t g) -> int64_t {  // first 16-byte block of row slice g's row
     return ((int64_t)p.base_off + row_of(g * RT + slot) * p.ldb + j0) >> 3;

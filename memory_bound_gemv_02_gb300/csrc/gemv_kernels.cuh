@@ -416,22 +416,45 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_rows_kernel(Params p) {
   }
 }
 
-// Second pass of split-K: c[row] = sum over segments s = 0 .. sg-1 (in that
-// order) of ws[s * n + row], rounded once to the output type.
+// Segments up to which the second pass of split-K gives each row one thread.
+constexpr int kReduceRowThreads = 32;
+
+// Second pass of split-K: c[row] = the sum over the sg segments of
+// ws[s * n + row], rounded once to the output type.  Up to
+// kReduceRowThreads segments, one thread adds a row's partials in segment
+// order; beyond that (long rows split into many segments) a warp takes the
+// row, lane l adding segments l, l + 32, ... in order, and the 32 lane sums
+// are combined by the fixed xor-shuffle tree.  Either way the order is fixed
+// for a given sg, so results are deterministic.
+template <class T, bool OUT_F32>
+__device__ __forceinline__ void store_reduced(void *c, int64_t row, float y) {
+  if (OUT_F32) {
+    static_cast<float *>(c)[row] = y;
+  } else {
+    static_cast<uint16_t *>(c)[row] = T::from_float(y);
+  }
+}
+
 template <class T, bool OUT_F32>
 __global__ void __launch_bounds__(256)
     gemv_splitk_reduce_kernel(const float *ws, void *c, int64_t n, int32_t sg, Epilogue ep) {
   allow_dependents();
   wait_for_predecessor();  // the partials come from the kernel before
-  for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < n;
-       row += (int64_t)gridDim.x * blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < sg; ++s) v += ws[(int64_t)s * n + row];
-    const float y = apply_epilogue<T>(ep, row, v);
-    if (OUT_F32) {
-      static_cast<float *>(c)[row] = y;
-    } else {
-      static_cast<uint16_t *>(c)[row] = T::from_float(y);
+  if (sg <= kReduceRowThreads) {
+    for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < n;
+         row += (int64_t)gridDim.x * blockDim.x) {
+      float v = 0.f;
+      for (int s = 0; s < sg; ++s) v += ws[(int64_t)s * n + row];
+      store_reduced<T, OUT_F32>(c, row, apply_epilogue<T>(ep, row, v));
+    }
+  } else {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < n; row += warps) {
+      float v = 0.f;
+      for (int s = lane; s < sg; s += 32) v += ws[(int64_t)s * n + row];
+      v = warp_sum(v);
+      if (lane == 0) store_reduced<T, OUT_F32>(c, row, apply_epilogue<T>(ep, row, v));
     }
   }
 }

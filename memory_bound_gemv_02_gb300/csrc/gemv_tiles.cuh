@@ -177,6 +177,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   // of B at a time across the GPU.
   const int64_t nloc = nr > cq ? (nr - cq + Cq - 1) / Cq : 0;
   const int64_t ngroups = (nloc + RT - 1) / RT;
+  if (ngroups == 0) {  // no rows for this CTA (a short row class): no staging, no loads
+    allow_dependents();
+    return;
+  }
   auto row_of = [&](int64_t m) -> int64_t { return NCLS * (cq + (int64_t)Cq * m) + cls; };
 
   auto rows_of = [&](int64_t g, int64_t (&g0)[R], bool (&valid)[R]) {

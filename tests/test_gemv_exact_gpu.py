@@ -184,7 +184,7 @@ def test_error_paths_launch_nothing(cuda_dev):
         g.gemv(B, a, c=B.view(-1)[:64])  # c inside B
     assert ei.value.status == g.GEMV_ERR_ALIAS
     with pytest.raises(g.GemvError) as ei:
-        g.gemv_ex(B, a, config={"grid_split": 100})
+        g.gemv_ex(B, a, config={"grid_split": 100000})  # more than 65536 k-segments
     assert ei.value.status == g.GEMV_ERR_CONFIG
     g.gemv_debug_inject(g.GEMV_ERR_CUDA)
     c = torch.full((64,), 3.0, dtype=torch.float16, device=cuda_dev)
@@ -373,3 +373,36 @@ def test_native_host_overhead_tool(cuda_dev):
     d = json.loads(r.stdout.strip().splitlines()[-1])
     assert 0 < d["gemv_us"] < 10.0
     assert 0 < d["empty_launch_us"] <= d["gemv_us"] + 1.0
+
+
+@pytest.mark.parametrize("n,k,dtype,cfg", [(2, 3_000_000, "f16", None), (3, 5_000_001, "bf16", None),
+                                           (2, 3_000_000, "bf16", {"variant": 4}), (64, 2**22, "f16", None)])
+def test_long_rows_against_oracle(cuda_dev, n, k, dtype, cfg):
+    """Rows longer than 64 segments of 32768 columns (thousands of k-segments
+    for the longest; the second pass then takes a warp per row)."""
+    B, a = inputs.make_inputs(n, k, dtype, "uniform", 11, cuda_dev)
+    for out_fp32 in (False, True):
+        c = _run(B, a, out_fp32, cfg)
+        check_against_oracle(c, B, a, out_fp32, label=f"{n}x{k} {dtype} {cfg} f32={out_fp32}")
+    assert g.gemv_last_config()["grid_split"] > 64
+
+
+def test_maximum_k_ones_closed_form(cuda_dev):
+    """n = 1, k = INT32_MAX (4 GiB of B and of a): with B = a = ones every
+    partial is exact, so the result is k rounded once -- 2^31 in fp32 and bf16,
+    +inf in fp16 (beyond 65504) -- the closed form c_i = k."""
+    k = 2**31 - 1
+    B = torch.ones((1, k), dtype=torch.float16, device=cuda_dev)
+    a = torch.ones(k, dtype=torch.float16, device=cuda_dev)
+    c32 = _run(B, a, True)
+    c16 = _run(B, a, False)
+    torch.cuda.synchronize()
+    assert g.gemv_last_config()["grid_split"] == 65536
+    assert c32.item() == float(2**31)
+    assert torch.isinf(c16).all() and c16.item() > 0
+    del B, a
+    Bb = torch.ones((1, k), dtype=torch.bfloat16, device=cuda_dev)
+    ab = torch.ones(k, dtype=torch.bfloat16, device=cuda_dev)
+    cb = _run(Bb, ab, False)
+    torch.cuda.synchronize()
+    assert (inputs.out_bits(cb) == oracle.round_out(np.array([float(k)]), "bf16")).all()

@@ -80,7 +80,7 @@ def test_forced_configs_are_honoured(gemv_lib, cfg):
 
 @pytest.mark.parametrize("cfg", [
     {"variant": 5}, {"rows_per_warp": 3}, {"warps_per_cta": 12}, {"warps_per_cta": 8, "warp_split": 3},
-    {"grid_split": 65}, {"variant": 2, "rows_per_warp": 2}, {"rows_per_warp": 2, "unroll": 8},
+    {"grid_split": 65537}, {"variant": 2, "rows_per_warp": 2}, {"rows_per_warp": 2, "unroll": 8},
 ])
 def test_invalid_forced_configs_rejected(gemv_lib, cfg):
     with pytest.raises(gemv_lib.GemvError) as ei:
@@ -350,3 +350,22 @@ def test_default_plan_replay_two_rows_and_split_k(gemv_lib, n, k, base_off, R):
     cfg = gemv_lib.gemv_plan(n, k, 0, base_off == 0, SM)
     assert cfg["rows_per_warp"] == R
     kernel_model.replay(n, k, cfg, base_off=base_off)
+
+
+@pytest.mark.parametrize("n,k,aligned", [(2, 3_000_000, True), (3, 5_000_001, False), (1, 2**31 - 1, False),
+                                         (64, 2**22, True), (1, 2**31 - 8, True)])
+def test_long_rows_plan(gemv_lib, n, k, aligned):
+    """k up to INT32_MAX: as many 32768-column segments as k needs (up to
+    65536), for both kernels."""
+    for variant in (0, 4):
+        cfg = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": variant} if variant else None)
+        assert cfg["k_segment"] <= 32768 and cfg["grid_split"] * cfg["k_segment"] >= k
+        assert (cfg["grid_split"] - 1) * cfg["k_segment"] < k
+        assert cfg["launches"] == 2 and cfg["ctas"] == cfg["row_blocks"] * cfg["grid_split"]
+
+
+@pytest.mark.parametrize("n,k,base_off", [(2, 3_000_000, 0), (3, 5_000_001, 3)])
+def test_long_rows_replay(gemv_lib, n, k, base_off):
+    for variant in (None, 4):
+        cfg = gemv_lib.gemv_plan(n, k, 0, base_off == 0, SM, config={"variant": variant} if variant else None)
+        kernel_model.replay(n, k, cfg, base_off=base_off)
