@@ -42,6 +42,13 @@ MUTANTS = {
     "gla_no_scale": ("o[h * dv + j] = scale * acc;", "o[h * dv + j] = acc;"),
     "gla_transposed_state": ("ref_load(S, (h * dk + i) * dv + j, fmt)", "ref_load(S, (h * dv + j) * dk + i, fmt)"),
     "gla_o_from_old_state": ("acc += qi * sn;", "acc += qi * sij;"),
+    "gla_decay_sign": ("const double decay = exp(ref_load(gk, h * dk + i, fmt));",
+                       "const double decay = exp(-ref_load(gk, h * dk + i, fmt));"),
+    "gla_q_for_k": ("const double kv = ref_load(k, h * dk + i, fmt)", "const double kv = ref_load(q, h * dk + i, fmt)"),
+    "gla_v_head_stride": ("ref_load(v, h * dv + j, fmt)", "ref_load(v, h * dk + j, fmt)"),
+    "gla_abs_sum_merged": ("ss[(h * dk + i) * dv + j] = fabs(decay * sij) + fabs(kv);",
+                           "ss[(h * dk + i) * dv + j] = fabs(decay * sij + kv);"),
+    "gla_abs_o_signed": ("acc_abs += fabs(qi * sn);", "acc_abs += qi * sn;"),
 }
 
 
@@ -126,10 +133,14 @@ def _check_gla(o):
     S = rng.integers(-3, 4, (bh, dk, dv)).astype(np.float64)
     for gk_val, decay in ((0.0, 1.0), (-np.inf, 0.0)):
         gk = np.full((bh, dk), gk_val)
-        S_new, out, _, _ = o.gla_ref_decode(bits(q), bits(k), bits(v), bits(gk), bits(S), 0.5, "f32")
-        want = decay * S + k[:, :, None] * v[:, None, :]
+        S_new, out, ss, os_ = o.gla_ref_decode(bits(q), bits(k), bits(v), bits(gk), bits(S), 0.5, "f32")
+        kv = k[:, :, None] * v[:, None, :]
+        want = decay * S + kv
         assert (S_new == want).all()
         assert (out == 0.5 * np.einsum("hi,hij->hj", q, want)).all()
+        # the magnitudes behind the tolerances, exact for these integers
+        assert (ss == np.abs(decay * S) + np.abs(kv)).all()
+        assert (os_ == 0.5 * np.einsum("hi,hij->hj", np.abs(q), np.abs(want))).all()
 
 
 PINS = [_check_decode, _check_encode, _check_closed_forms, _check_bruteforce, _check_epilogue, _check_gla]
