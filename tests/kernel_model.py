@@ -350,15 +350,23 @@ def staged_shifted(a, j0, seglen, off, as_elems):
 
 
 
-def gla_heads_per_cta(bh, dk, cpr, threads=256, rows_in_flight=4):
+def gla_rows_in_flight(dk, cpr):
+    """The host's choice of rows in flight per thread: 8 for heads of at most
+    1024 16-byte chunks, else 4."""
+    return 8 if dk * cpr <= 1024 else 4
+
+
+def gla_heads_per_cta(bh, dk, cpr, threads=256, rows_in_flight=None):
     """The host's choice of heads processed side by side per CTA round."""
+    if rows_in_flight is None:
+        rows_in_flight = gla_rows_in_flight(dk, cpr)
     G = 1
     while 2 * G * cpr <= threads and 2 * G <= bh and dk * cpr * 2 * G <= rows_in_flight * threads:
         G *= 2
     return G
 
 
-def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=4, grid=None):
+def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=None, grid=None):
     """Index replay of ``gla_decode_kernel`` (G heads per CTA round): every
     state element of every head is read and written exactly once by one
     thread, every staging, partial and output index is in range, and every
@@ -367,6 +375,8 @@ def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=4, grid=None)
     assert dv % vec == 0
     cpr = dv // vec
     assert 1 <= cpr <= threads
+    if rows_in_flight is None:
+        rows_in_flight = gla_rows_in_flight(dk, cpr)
     G = gla_heads_per_cta(bh, dk, cpr, threads, rows_in_flight)
     assert G * cpr <= threads and threads % G == 0
     TPG = threads // G

@@ -227,8 +227,10 @@ def test_gla_heads_per_cta_choice():
     """Small heads are processed several per CTA round (about 4 rows per
     thread), large ones one per round."""
     hp = kernel_model.gla_heads_per_cta
-    assert hp(4096, 64, 8) == 2 and hp(16384, 16, 8) == 8 and hp(2048, 128, 16) == 1
+    assert kernel_model.gla_rows_in_flight(64, 8) == 8 and kernel_model.gla_rows_in_flight(128, 16) == 4
+    assert hp(4096, 64, 8) == 4 and hp(16384, 16, 8) == 16 and hp(2048, 128, 16) == 1
     assert hp(1024, 256, 32) == 1 and hp(1, 16, 8) == 1 and hp(3, 16, 8) == 2
+    assert hp(4096, 64, 8, rows_in_flight=4) == 2
 
 
 # ------------------------------------------------------------- bulk variant --
