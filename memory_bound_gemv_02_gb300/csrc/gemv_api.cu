@@ -645,6 +645,8 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   gemv_config cfg{};
   float *ws = nullptr;
   MainKernel mk = nullptr;
+  bool defer = false;        // keep row results in shared memory, store after one wait
+  int64_t launch_smem = 0;   // dynamic shared memory of the launch
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const DeviceInfo &di = device_info_locked(dev);
@@ -667,10 +669,24 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
         g_cache.emplace(key, cfg);
       }
     }
+    launch_smem = cfg.smem_bytes;
     if (cfg.smem_bytes > di.max_smem_optin) return GEMV_ERR_CONFIG;
+    // Shared input vector promised (B and a unwritten by the work in
+    // flight): the tiles kernel keeps its row results (at most
+    // kDeferMaxRows per CTA) and writes them after one wait at the end, so
+    // it streams all of B while the preceding kernel drains.
+    if (overlap == GEMV_OVERLAP_PDL_PREFETCH_BA && cfg.variant == GEMV_VARIANT_TILES) {
+      const int NCLS = aligned ? 1 : 8;
+      const int64_t nloc_max = cdiv(cdiv(n, NCLS), (int64_t)cfg.row_blocks / NCLS);
+      const int64_t extra = round_up(nloc_max * 4, 16);
+      if (nloc_max <= kDeferMaxRows && cfg.smem_bytes + extra <= di.max_smem_optin) {
+        defer = true;
+        launch_smem = cfg.smem_bytes + extra;
+      }
+    }
     mk = lookup_main(dtype, cfg, aligned, !is_identity(ep));
     if (mk == nullptr) return GEMV_ERR_CONFIG;
-    e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
+    e = ensure_smem_attr_locked((const void *)mk, dev, (int)launch_smem);
     if (e != cudaSuccess) return cuda_fail(e);
     if (cfg.grid_split > 1) {
       st = workspace_locked(dev, stream, (size_t)cfg.grid_split * (size_t)n * sizeof(float), &ws);
@@ -704,7 +720,8 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   }
   p.flags = ((overlap >= GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
             ((overlap == GEMV_OVERLAP_PDL_PREFETCH_BA) ? kFlagPrefetchA : 0) |
-            (is_identity(ep) ? 0 : kFlagEpilogue) | (cfg.l2_prefetch << kFlagL2Shift);
+            (is_identity(ep) ? 0 : kFlagEpilogue) | (defer ? kFlagDeferStores : 0) |
+            (cfg.l2_prefetch << kFlagL2Shift);
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -712,7 +729,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)cfg.ctas);
   lc.blockDim = dim3((unsigned)(cfg.warps_per_cta * 32));
-  lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
+  lc.dynamicSmemBytes = (size_t)launch_smem;
   lc.stream = stream;
   lc.attrs = attr;
   lc.numAttrs = overlap != GEMV_OVERLAP_NONE ? 1 : 0;

@@ -77,6 +77,8 @@ constexpr int kFlagPrefetchB = 1;
 constexpr int kFlagL2Shift = 1;  // 2 bits: tile rounds of bulk L2 prefetch ahead
 constexpr int kFlagPrefetchA = 8;   // stage a before waiting on the predecessor
 constexpr int kFlagEpilogue = 16;   // the fused epilogue is not the identity
+constexpr int kFlagDeferStores = 32;  // tiles kernel with kFlagPrefetchA: keep row results, store after one wait
+constexpr int64_t kDeferMaxRows = 4096;  // most rows per CTA whose results are kept (16 KB of shared memory)
 constexpr int kWaitPolls = 1 << 20;  // default bound on the polls of one mbarrier wait
 
 // Shared-memory layout of the bulk kernel, in bytes from the start of the

@@ -225,12 +225,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   for (int m = 1; m <= pf; ++m) prefetch_tile(m);
   // a is staged before the wait only when the caller promised that the
   // predecessor does not write it (kFlagPrefetchA); c is always written
-  // after the wait.
+  // after the wait.  With kFlagDeferStores (only set with kFlagPrefetchA)
+  // the CTA's row results are kept in shared memory and written after a
+  // single wait at the end: the whole stream of B then overlaps the
+  // preceding kernel's drain.
   const bool early_a = early && (p.flags & kFlagPrefetchA) != 0;
+  const bool defer = early_a && (p.flags & kFlagDeferStores) != 0;
+  float *res = ps + 2 * W * R;  // [nloc] row results when deferring
   if (early && !early_a) wait_for_predecessor();
   stage_a_shifted(p, as4, j0, len, off);
   __syncthreads();
-  if (early_a) wait_for_predecessor();
+  if (early_a && !defer) wait_for_predecessor();
 
   int buf = 0;
   for (int64_t g = 0; g < ngroups; ++g) {
@@ -265,7 +270,13 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
       if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
-          if (valid[r]) store_out<T, OUT_F32, EPI>(p, gs, row_of(mb + r), v[r]);
+          if (valid[r]) {
+            if (defer) {
+              res[mb + r] = v[r];
+            } else {
+              store_out<T, OUT_F32, EPI>(p, gs, row_of(mb + r), v[r]);
+            }
+          }
       }
     } else {
       float *pb = ps + buf * (W * R);
@@ -279,11 +290,20 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
         if (m < nloc) {
           float sum = 0.f;
           for (int s2 = 0; s2 < S; ++s2) sum += pb[(slot * R + lane) * S + s2];
-          store_out<T, OUT_F32, EPI>(p, gs, row_of(m), sum);
+          if (defer) {
+            res[m] = sum;
+          } else {
+            store_out<T, OUT_F32, EPI>(p, gs, row_of(m), sum);
+          }
         }
       }
       buf ^= 1;
     }
+  }
+  if (defer) {
+    wait_for_predecessor();
+    __syncthreads();
+    for (int64_t m = threadIdx.x; m < nloc; m += blockDim.x) store_out<T, OUT_F32, EPI>(p, gs, row_of(m), res[m]);
   }
 }
 

@@ -28,7 +28,7 @@ NS = [1, 2, 7, 31, 64, 97, 256, 513, 1000, 2048, 3001]
 KS = [1, 3, 8, 17, 64, 100, 513, 1031, 4096, 4099, 7169, 16384, 33000]
 CONFIGS = [None, {"variant": 3}, {"variant": 4}, {"variant": 2}, {"grid_split": 3}, {"warp_split": 2},
            {"variant": 4, "stages": 3}, {"overlap": 2}, {"overlap": 0}, {"variant": 3, "rows_per_warp": 2, "unroll": 4},
-           {"variant": 4, "warp_split": 4, "overlap": 3}]
+           {"variant": 4, "warp_split": 4, "overlap": 3}, {"overlap": 3}, {"variant": 3, "warp_split": 2, "overlap": 3}]
 ACTS = [None, None, "relu", "sigmoid", "silu"]
 SLOPE = {None: 1.0, "none": 1.0, "relu": 1.0, "sigmoid": 0.25, "silu": 1.1}
 

@@ -19,7 +19,7 @@ import torch
 
 import memory_bound_gemv_02_gb300 as g
 import oracle
-from gpu_helpers import check_against_oracle, exact_bits_match, oracle_for
+from gpu_helpers import check_against_oracle, exact_bits_match, oracle_for, sample_rows
 from memory_bound_gemv_02_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -406,3 +406,26 @@ def test_maximum_k_ones_closed_form(cuda_dev):
     cb = _run(Bb, ab, False)
     torch.cuda.synchronize()
     assert (inputs.out_bits(cb) == oracle.round_out(np.array([float(k)]), "bf16")).all()
+
+
+@pytest.mark.parametrize("n,k,dtype", [(3000, 4104, "bf16"), (1_400_000, 16, "f16"), (513, 7169, "f16")])
+def test_shared_input_deferred_stores(cuda_dev, n, k, dtype):
+    """GEMV_OVERLAP_PDL_PREFETCH_BA: the tiles kernel keeps its row results
+    in shared memory and stores them after one wait (up to 4096 rows per
+    CTA; beyond that, as 1.4M rows of 16 here, it stores as it goes).  A
+    chain of calls sharing a, each writing the same c and then its own,
+    all checked."""
+    cfg = {"overlap": 3, "variant": 3}
+    _, a = inputs.make_inputs(1, k, dtype, "uniform", 12, cuda_dev)
+    Bs = [inputs.make_inputs(n, k, dtype, "uniform", 30 + i, cuda_dev)[0] for i in range(3)]
+    c = torch.empty(n, dtype=Bs[0].dtype, device=cuda_dev)
+    outs = []
+    for _ in range(2):
+        for B in Bs:
+            g.gemv_ex(B, a, c=c, config=cfg)
+            outs.append(g.gemv_ex(B, a, config=cfg))
+    torch.cuda.synchronize()
+    rows = sample_rows(n, 160)
+    check_against_oracle(c, Bs[-1], a, False, rows=rows, label="last writer of c")
+    for i, o in enumerate(outs[:3]):
+        check_against_oracle(o, Bs[i], a, False, rows=rows, label=f"shared input B{i}")
