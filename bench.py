@@ -523,11 +523,13 @@ def run_gla(args, dev):
             q, k, v, gk, S = (x.to(tdt[dt]) for x in (q, k, v, gk, S))
             o = torch.empty((bh, dv), dtype=tdt[dt], device=dev)
             sets.append((q, k, v, gk, S, o))
-        def timed(variant):
+        S_outs = [torch.empty_like(x[4]) for x in sets]
+
+        def timed(variant, flags=0, out_of_place=False):
             calls = [(L.gla_decode_ex, (q.data_ptr(), k.data_ptr(), v.data_ptr(), gk.data_ptr(), S.data_ptr(),
-                                        S.data_ptr(), o.data_ptr(), bh, dk, dv, ctypes.c_float(dk ** -0.5),
-                                        code[dt], variant, s))
-                     for q, k, v, gk, S, o in sets]
+                                        (S_out if out_of_place else S).data_ptr(), o.data_ptr(), bh, dk, dv,
+                                        ctypes.c_float(dk ** -0.5), code[dt], variant, flags, s))
+                     for (q, k, v, gk, S, o), S_out in zip(sets, S_outs)]
             if calls[0][0](*calls[0][1]) != 0:
                 return None
             _, per = time_calls(L, calls, s, args.gla_steps, 10)
@@ -539,13 +541,19 @@ def run_gla(args, dev):
              "us_isolated_median": round(iso, 3), "us_back_to_back": round(b2b, 3),
              "gbs_back_to_back": round(nbytes / b2b / 1e3, 1), "gbs_isolated": round(nbytes / iso / 1e3, 1),
              "pct_of_8tbps": round(100 * nbytes / b2b / 1e3 / NOMINAL_HBM_GBS, 1), "state_copies": copies}
-        # each kernel layout forced, for comparison
+        # each kernel layout forced, for comparison; and the state requested
+        # before the wait, against the same calls without it.  Those write
+        # S_new to a second copy of each state instead of S, so that no call
+        # in flight writes a state any call reads (the flag's promise).
         for name, variant in (("cta", g.GLA_VARIANT_CTA), ("warp", g.GLA_VARIANT_WARP)):
             t = timed(variant)
             r[f"us_back_to_back_{name}"] = None if t is None else round(t[1], 3)
+        for name, flags in (("out_of_place", 0), ("prefetch_state", g.GLA_PREFETCH_STATE)):
+            t = timed(g.GLA_VARIANT_AUTO, flags, out_of_place=True)
+            r[f"us_back_to_back_{name}"] = None if t is None else round(t[1], 3)
         out.append(r)
         print(json.dumps(r), file=sys.stderr, flush=True)
-        del sets
+        del sets, S_outs
         torch.cuda.empty_cache()
     print(json.dumps({"gla_decode": out}), flush=True)
     return 0

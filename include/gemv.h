@@ -91,6 +91,12 @@ enum {
                                  while the preceding kernel drains; it waits for that
                                  kernel's completion (and its memory) before reading or
                                  writing any global memory */
+  /* "Work still running on the stream", for the two promises below: every
+     kernel launched on the stream after its last ordinary operation (a kernel
+     launched without the programmatic-serialization attribute, a copy, a memset
+     or an event wait).  This library's kernels let their successor start before
+     they wait for their own predecessor, so a chain of them may all run at
+     once; an ordinary operation completes only after everything before it. */
   GEMV_OVERLAP_PDL_PREFETCH_B = 2, /* as GEMV_OVERLAP_PDL, and each CTA streams its first tile
                                  of B into registers (bulk variant: its first ring buffers
                                  into shared memory) before waiting.  The caller guarantees
@@ -390,9 +396,21 @@ enum {
                                dv * element size <= 512 bytes */
 };
 
+/* Flags of gla_decode_ex(). */
+enum {
+  GLA_PREFETCH_STATE = 1 /* the caller guarantees that no work still running on the stream (as
+                            defined for GEMV_OVERLAP_PDL_PREFETCH_B) writes S: true when each layer
+                            of a decoder owns its state and an ordinary operation (sampling, a copy)
+                            separates one token's layers from the next token's.  The CTA layout then
+                            requests its first state rows before waiting for the preceding kernel;
+                            q, k, v, gk, S_new and o are still accessed only after the wait.  The
+                            warp layout ignores the flag */
+};
+
 /*
  * gla_decode() with the kernel layout chosen by the caller (`variant`,
- * GLA_VARIANT_*).  The automatic choice is GLA_VARIANT_CTA, which takes
+ * GLA_VARIANT_*) and launch flags (`flags`, GLA_PREFETCH_STATE or 0;
+ * unknown bits return GEMV_ERR_ARG).  The automatic choice is GLA_VARIANT_CTA, which takes
  * several small heads side by side per round (measured faster than a warp
  * per head on every workload tried).  GEMV_ERR_CONFIG for a layout the shape
  * does not allow;
@@ -400,7 +418,7 @@ enum {
  * identically; o differs only by the order of its fp32 sum.
  */
 int gla_decode_ex(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
-                  void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, int variant,
+                  void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, int variant, int flags,
                   cudaStream_t stream);
 
 #ifdef __cplusplus

@@ -37,6 +37,7 @@ GEMV_ACT_NONE, GEMV_ACT_RELU, GEMV_ACT_SIGMOID, GEMV_ACT_SILU = 0, 1, 2, 3
 GEMV_BIAS_INPUT_TYPE, GEMV_BIAS_F32 = 0, 1
 GLA_F16, GLA_BF16, GLA_F32 = 0, 1, 2
 GLA_VARIANT_AUTO, GLA_VARIANT_CTA, GLA_VARIANT_WARP = 0, 1, 2
+GLA_PREFETCH_STATE = 1
 _GLA_DTYPE = {torch.float16: GLA_F16, torch.bfloat16: GLA_BF16, torch.float32: GLA_F32}
 ACTIVATIONS = {"none": GEMV_ACT_NONE, "relu": GEMV_ACT_RELU, "sigmoid": GEMV_ACT_SIGMOID, "silu": GEMV_ACT_SILU}
 
@@ -112,7 +113,7 @@ def lib() -> ctypes.CDLL:
             L.gemv_wait_timeouts.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32)]
             L.gemv_debug_wait_budget.argtypes = [ctypes.c_int32]
             L.gla_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, i32, vp]
-            L.gla_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, i32, i32, vp]
+            L.gla_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, i32, i32, i32, vp]
             for name in ENTRY_POINTS:
                 if name != "gemv_status_string":
                     getattr(L, name).restype = i32
@@ -343,12 +344,13 @@ def gemv_debug_wait_budget(polls: int) -> None:
     _check(lib().gemv_debug_wait_budget(int(polls)), "gemv_debug_wait_budget")
 
 
-def gla_decode(q, k, v, gk, S, scale: float, S_new=None, o=None, stream=None, variant: int = 0):
+def gla_decode(q, k, v, gk, S, scale: float, S_new=None, o=None, stream=None, variant: int = 0, flags: int = 0):
     """One gated-linear-attention decode step for bh heads: S_new =
     diag(exp(gk)) S + outer(k, v), o = scale * q^T S_new.  Shapes: q, k, gk
     (bh, dk); v (bh, dv); S (bh, dk, dv); one dtype (fp16, bf16 or fp32).
     ``S_new`` may be ``S`` (in place).  ``variant``: GLA_VARIANT_* (0: the
-    library's choice; calls ``gla_decode_ex``).  Returns (S_new, o)."""
+    library's choice); ``flags``: GLA_PREFETCH_STATE when no work in flight
+    writes S (either calls ``gla_decode_ex``).  Returns (S_new, o)."""
     bh, dk, dv = S.shape
     if q.shape != (bh, dk) or k.shape != (bh, dk) or gk.shape != (bh, dk) or v.shape != (bh, dv):
         raise ValueError("shape mismatch")
@@ -367,8 +369,8 @@ def gla_decode(q, k, v, gk, S, scale: float, S_new=None, o=None, stream=None, va
     with torch.cuda.device(S.device):
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), gk.data_ptr(), S.data_ptr(), S_new.data_ptr(),
                 o.data_ptr(), bh, dk, dv, float(scale), _GLA_DTYPE[dt])
-        if variant:
-            st = lib().gla_decode_ex(*args, int(variant), _stream_handle(stream))
+        if variant or flags:
+            st = lib().gla_decode_ex(*args, int(variant), int(flags), _stream_handle(stream))
         else:
             st = lib().gla_decode(*args, _stream_handle(stream))
     _check(st, "gla_decode")

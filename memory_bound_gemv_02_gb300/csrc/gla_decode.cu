@@ -38,6 +38,7 @@ struct GlaParams {
   int32_t dk, dv;
   float scale;
   int32_t heads_per_cta;  // gla_decode_kernel: heads processed side by side per round (G)
+  int32_t early_state;    // GLA_PREFETCH_STATE: S is unwritten by the work in flight
 };
 
 struct F32 {};  // tag of the fp32 storage type
@@ -134,9 +135,12 @@ __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
   const int t = threadIdx.x;
   const int gi = t / TPG, tl = t % TPG;   // head slot of this thread, its index in the slot
   // Launched as a programmatic dependent launch: let the next kernel be
-  // scheduled early, and touch no memory before the previous one is done.
+  // scheduled early, and touch no memory before the previous one is done --
+  // except, with GLA_PREFETCH_STATE, the first state rows of the first
+  // round, which the caller promised no work in flight writes.
   allow_dependents();
-  wait_for_predecessor();
+  bool waited = p.early_state == 0;
+  if (waited) wait_for_predecessor();
   const int cc = tl % cpr, rl = tl / cpr;
   const int64_t rounds = (p.bh + G - 1) / G;
 
@@ -153,6 +157,10 @@ __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
     for (int u = 0; u < RIF; ++u) {
       const int i = rl + u * RP;
       sv[u] = (active && i < dk) ? ldg_stream(Srow + (int64_t)i * cpr) : zero4();
+    }
+    if (!waited) {
+      wait_for_predecessor();
+      waited = true;
     }
     for (int x = t; x < nh * dk; x += kGlaThreads) {
       dec[x] = expf(IO::scalar(p.gk, h0 * dk + x));
@@ -322,8 +330,9 @@ using namespace gemvk;
 
 extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const void *gk, const void *S,
                              void *S_new, void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype,
-                             int variant, cudaStream_t stream) {
+                             int variant, int flags, cudaStream_t stream) {
   if (dtype != GLA_F16 && dtype != GLA_BF16 && dtype != GLA_F32) return GEMV_ERR_DTYPE;
+  if (flags & ~GLA_PREFETCH_STATE) return GEMV_ERR_ARG;
   if (variant < GLA_VARIANT_AUTO || variant > GLA_VARIANT_WARP) return GEMV_ERR_CONFIG;
   if (bh < 0 || dk < 0 || dv < 0 || dk > kGlaMaxDk) return GEMV_ERR_ARG;
   if (bh == 0 || dv == 0) return GEMV_OK;
@@ -368,6 +377,7 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
   GlaParams p;
   p.q = q; p.k = k; p.v = v; p.gk = gk; p.S = S; p.S_new = S_new; p.o = o;
   p.bh = bh; p.dk = (int32_t)dk; p.dv = (int32_t)dv; p.scale = scale; p.heads_per_cta = 1;
+  p.early_state = (flags & GLA_PREFETCH_STATE) ? 1 : 0;
   if (variant == GLA_VARIANT_WARP) {
     void (*fw)(GlaParams) = dtype == GLA_F16 ? gla_decode_warp_kernel<F16>
                             : dtype == GLA_BF16 ? gla_decode_warp_kernel<BF16> : gla_decode_warp_kernel<F32>;
@@ -421,5 +431,5 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
 
 extern "C" int gla_decode(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
                           void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, cudaStream_t stream) {
-  return gla_decode_ex(q, k, v, gk, S, S_new, o, bh, dk, dv, scale, dtype, GLA_VARIANT_AUTO, stream);
+  return gla_decode_ex(q, k, v, gk, S, S_new, o, bh, dk, dv, scale, dtype, GLA_VARIANT_AUTO, 0, stream);
 }

@@ -181,3 +181,48 @@ def test_gla_empty_dk_and_errors(cuda_dev):
         g.gla_decode(q, k, torch.zeros((2, 32), dtype=torch.bfloat16, device=cuda_dev), gk, S0, scale=1.0,
                      S_new=S1)
     assert ei.value.status == g.GEMV_ERR_ALIAS
+
+
+@pytest.mark.parametrize("variant", [g.GLA_VARIANT_AUTO, g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+@pytest.mark.parametrize("bh,d,dtype", [(64, 64, torch.bfloat16), (300, 128, torch.float16), (48, 32, torch.float32)])
+def test_gla_prefetch_state_layer_chain(cuda_dev, variant, bh, d, dtype):
+    """GLA_PREFETCH_STATE over a stack of layers, each owning its state: step
+    t of layer l follows step t of layer l-1 on the stream and reads that
+    step's o as its v, so only the state may be requested before the wait.
+    An ordinary kernel separates one step's layers from the next step's (the
+    promise's condition: the last write of a layer's state has completed).
+    Every step is checked against the oracle on the values it read."""
+    layers, steps, scale = 4, 3, d ** -0.5
+    states = [_make(bh, d, d, dtype, 40 + l, cuda_dev)[4] for l in range(layers)]
+    for t in range(steps):
+        _, _, v, _, _ = _make(bh, d, d, dtype, 200 + t, cuda_dev)
+        for l in range(layers):
+            q, k, _, gk, _ = _make(bh, d, d, dtype, 300 + 10 * t + l, cuda_dev)
+            S_prev = states[l].clone()
+            _, o = g.gla_decode(q, k, v, gk, states[l], scale=scale, S_new=states[l], variant=variant,
+                                flags=g.GLA_PREFETCH_STATE)
+            _check(q, k, v, gk, S_prev, states[l], o, scale, f"step {t} layer {l}")
+            v = o
+    # without the checks in between: the same chain back to back, compared
+    # with a run that waits before every access
+    for flags in (g.GLA_PREFETCH_STATE, 0):
+        st = [_make(bh, d, d, dtype, 40 + l, cuda_dev)[4] for l in range(layers)]
+        ins = [_make(bh, d, d, dtype, 500 + l, cuda_dev) for l in range(layers)]
+        v = ins[0][2]
+        for t in range(steps):
+            v = v * 1  # an ordinary launch between steps
+            for l in range(layers):
+                q, k, _, gk, _ = ins[l]
+                _, v = g.gla_decode(q, k, v, gk, st[l], scale=scale, S_new=st[l], variant=variant, flags=flags)
+        torch.cuda.synchronize()
+        if flags:
+            want = (v.clone(), [x.clone() for x in st])
+    assert torch.equal(_t(v), _t(want[0])) and all(torch.equal(_t(a), _t(b)) for a, b in zip(st, want[1]))
+
+
+def test_gla_flags_rejected(cuda_dev):
+    q, k, v, gk, S = _make(2, 16, 24, torch.bfloat16, 1, cuda_dev)
+    for bad in (2, 1 << 8, -1):
+        with pytest.raises(g.GemvError) as ei:
+            g.gla_decode(q, k, v, gk, S, scale=1.0, flags=bad)
+        assert ei.value.status == g.GEMV_ERR_ARG
