@@ -545,7 +545,7 @@ def run_gla(args, dev):
         # before the wait, against the same calls without it.  Those write
         # S_new to a second copy of each state instead of S, so that no call
         # in flight writes a state any call reads (the flag's promise).
-        for name, variant in (("cta", g.GLA_VARIANT_CTA), ("warp", g.GLA_VARIANT_WARP)):
+        for name, variant in (("cta", g.GLA_VARIANT_CTA), ("warp", g.GLA_VARIANT_WARP), ("pipe", g.GLA_VARIANT_PIPE)):
             t = timed(variant)
             r[f"us_back_to_back_{name}"] = None if t is None else round(t[1], 3)
         for name, flags in (("out_of_place", 0), ("prefetch_state", g.GLA_PREFETCH_STATE)):

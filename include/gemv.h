@@ -90,7 +90,9 @@ enum {
                                  use) programmatic dependent launch: the kernel may be scheduled
                                  while the preceding kernel drains; it waits for that
                                  kernel's completion (and its memory) before reading or
-                                 writing any global memory */
+                                 writing any global memory.  Before the wait it only asks L2
+                                 to prefetch its first tile of B: a hint, which reads nothing
+                                 into the kernel and needs no promise */
   /* "Work still running on the stream", for the two promises below: every
      kernel launched on the stream after its last ordinary operation (a kernel
      launched without the programmatic-serialization attribute, a copy, a memset
@@ -391,9 +393,15 @@ enum {
                                more for small ones: about 4 rows per thread): 16-byte column chunks
                                of 4 rows in flight per thread, row-block partials of o added in
                                shared memory */
-  GLA_VARIANT_WARP = 2      /* one warp per head: lanes own (row group, column chunk) pairs, 8 rows
+  GLA_VARIANT_WARP = 2,     /* one warp per head: lanes own (row group, column chunk) pairs, 8 rows
                                in flight per lane, o reduced by warp shuffles; needs
                                dv * element size <= 512 bytes */
+  GLA_VARIANT_PIPE = 3      /* GLA_VARIANT_CTA with the next round (its state, q, k, gk, v) copied
+                               into a second shared-memory buffer by asynchronous copies while the
+                               current round computes; needs dk * element size a multiple of 16,
+                               q, k, gk 16-byte aligned, dk * dv * element size <= 32 KiB and its
+                               two buffers within 75 KiB of shared memory.  S_new bit-identical to
+                               GLA_VARIANT_CTA; o too where both take the same heads per round */
 };
 
 /* Flags of gla_decode_ex(). */
@@ -404,18 +412,21 @@ enum {
                             separates one token's layers from the next token's.  The CTA layout then
                             requests its first state rows before waiting for the preceding kernel;
                             q, k, v, gk, S_new and o are still accessed only after the wait.  The
-                            warp layout ignores the flag */
+                            warp layout ignores the flag.  Without it, the pipelined layout only
+                            asks L2 to prefetch its first state rows before the wait (a hint,
+                            which reads nothing into the kernel) */
 };
 
 /*
  * gla_decode() with the kernel layout chosen by the caller (`variant`,
  * GLA_VARIANT_*) and launch flags (`flags`, GLA_PREFETCH_STATE or 0;
- * unknown bits return GEMV_ERR_ARG).  The automatic choice is GLA_VARIANT_CTA, which takes
- * several small heads side by side per round (measured faster than a warp
+ * unknown bits return GEMV_ERR_ARG).  The automatic choice is GLA_VARIANT_PIPE
+ * where the shape and alignment allow it, else GLA_VARIANT_CTA (both take
+ * several small heads side by side per round; measured faster than a warp
  * per head on every workload tried).  GEMV_ERR_CONFIG for a layout the shape
- * does not allow;
- * otherwise as gla_decode().  The two layouts compute every S_new element
- * identically; o differs only by the order of its fp32 sum.
+ * does not allow; otherwise as gla_decode().  All layouts compute every S_new
+ * element identically; o differs between the warp layout and the CTA layouts
+ * only by the order of its fp32 sum.
  */
 int gla_decode_ex(const void *q, const void *k, const void *v, const void *gk, const void *S, void *S_new,
                   void *o, int64_t bh, int64_t dk, int64_t dv, float scale, int dtype, int variant, int flags,

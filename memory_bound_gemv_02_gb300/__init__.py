@@ -36,7 +36,7 @@ GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B, GEMV_OVERLAP_P
 GEMV_ACT_NONE, GEMV_ACT_RELU, GEMV_ACT_SIGMOID, GEMV_ACT_SILU = 0, 1, 2, 3
 GEMV_BIAS_INPUT_TYPE, GEMV_BIAS_F32 = 0, 1
 GLA_F16, GLA_BF16, GLA_F32 = 0, 1, 2
-GLA_VARIANT_AUTO, GLA_VARIANT_CTA, GLA_VARIANT_WARP = 0, 1, 2
+GLA_VARIANT_AUTO, GLA_VARIANT_CTA, GLA_VARIANT_WARP, GLA_VARIANT_PIPE = 0, 1, 2, 3
 GLA_PREFETCH_STATE = 1
 _GLA_DTYPE = {torch.float16: GLA_F16, torch.bfloat16: GLA_BF16, torch.float32: GLA_F32}
 ACTIVATIONS = {"none": GEMV_ACT_NONE, "relu": GEMV_ACT_RELU, "sigmoid": GEMV_ACT_SIGMOID, "silu": GEMV_ACT_SILU}

@@ -721,7 +721,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
   p.flags = ((overlap >= GEMV_OVERLAP_PDL_PREFETCH_B) ? kFlagPrefetchB : 0) |
             ((overlap == GEMV_OVERLAP_PDL_PREFETCH_BA) ? kFlagPrefetchA : 0) |
             (is_identity(ep) ? 0 : kFlagEpilogue) | (defer ? kFlagDeferStores : 0) |
-            (cfg.l2_prefetch << kFlagL2Shift);
+            ((overlap == GEMV_OVERLAP_PDL) ? kFlagL2First : 0) | (cfg.l2_prefetch << kFlagL2Shift);
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -152,10 +152,18 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_bulk_kernel(const Params 
 
   // The first NS chunks go out before a is staged (and, under a programmatic
   // dependent launch with kFlagPrefetchB, before the preceding kernel has
-  // finished: B is then promised read-only).
+  // finished: B is then promised read-only).  Without that promise
+  // (kFlagL2First), lane 0 only asks L2 for those chunks' blocks before
+  // waiting: a prefetch reads nothing into the kernel.
   allow_dependents();
   const bool early = (p.flags & kFlagPrefetchB) != 0;
-  if (!early) wait_for_predecessor();
+  if (!early) {
+    if ((p.flags & kFlagL2First) && lane == 0 && gv > 0 && t1 > t0) {
+      const int nb = (t1 - t0) < NS * SB ? (t1 - t0) : NS * SB;
+      prefetch_l2(bal + block_of(0) + t0, (uint32_t)nb * 16u);
+    }
+    wait_for_predecessor();
+  }
   if (lane == 0) {
     while (ic < total && ic < NS) issue_next();
   }

@@ -78,6 +78,7 @@ constexpr int kFlagL2Shift = 1;  // 2 bits: tile rounds of bulk L2 prefetch ahea
 constexpr int kFlagPrefetchA = 8;   // stage a before waiting on the predecessor
 constexpr int kFlagEpilogue = 16;   // the fused epilogue is not the identity
 constexpr int kFlagDeferStores = 32;  // tiles kernel with kFlagPrefetchA: keep row results, store after one wait
+constexpr int kFlagL2First = 64;      // without kFlagPrefetchB: ask L2 for the first tile of B before the wait
 constexpr int64_t kDeferMaxRows = 4096;  // most rows per CTA whose results are kept (16 KB of shared memory)
 constexpr int kWaitPolls = 1 << 20;  // default bound on the polls of one mbarrier wait
 

@@ -209,10 +209,21 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   // stream starts at once and the staging latency hides under it.  Under a
   // programmatic dependent launch with kFlagPrefetchB they even go out
   // before the preceding kernel has finished (B is then promised read-only);
-  // a and c are touched only after wait_for_predecessor().
+  // a and c are touched only after wait_for_predecessor().  Without that
+  // promise (kFlagL2First), each warp only asks L2 for the blocks of its
+  // first loads before waiting: a prefetch reads nothing into the kernel,
+  // and L2 is where the preceding kernel's writes land, so no write can be
+  // missed.
   allow_dependents();
   const bool early = (p.flags & kFlagPrefetchB) != 0;
-  if (!early) wait_for_predecessor();
+  if (!early) {
+    if ((p.flags & kFlagL2First) && lane < R && t1 > t0 && (int64_t)slot * R + lane < nloc) {
+      const int64_t gb = ((int64_t)p.base_off + row_of((int64_t)slot * R + lane) * p.ldb + j0) >> 3;
+      const int nb = (t1 - t0) < 32 * U ? (t1 - t0) : 32 * U;
+      prefetch_l2(bal + gb + t0, (uint32_t)nb * 16u);
+    }
+    wait_for_predecessor();
+  }
   uint4 bv[U][R];
   bool prefetched = false;
   if (ngroups > 0) {

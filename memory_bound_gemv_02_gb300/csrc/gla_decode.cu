@@ -18,7 +18,9 @@
 // (unrounded) for their columns.  The RP row partials of each column are
 // added in shared memory in row-block order, so the result is deterministic.
 // Four rows are in flight per thread; the first four are requested before
-// the round's staging, so their latency overlaps it.
+// the round's staging, so their latency overlaps it.  A pipelined form
+// (gla_decode_pipe_kernel) copies the next round into shared memory while
+// the current one computes.
 // S_new may be S itself (an in-place step): every element is read and then
 // written by the same thread.
 #include <cuda_runtime.h>
@@ -119,6 +121,31 @@ __device__ __forceinline__ void stg_stream(uint4 *p, const uint4 &v) {
                : "memory");
 }
 
+// Ask L2 for bytes [p, p + min(bytes, 32 * 16 KB)), a multiple of 16, in
+// pieces of at most 16 KB, piece i by lane i of the calling warp.  Issued
+// before waiting on the preceding kernel: a prefetch reads nothing into the
+// kernel, and L2 is where that kernel's writes land, so it needs no promise.
+constexpr int64_t kGlaL2Piece = 16 * 1024;
+__device__ __forceinline__ void prefetch_l2_pieces(const void *p, int64_t bytes, int lane) {
+  const int64_t off = (int64_t)lane * kGlaL2Piece;
+  if (off < bytes) {
+    const int64_t nb = bytes - off < kGlaL2Piece ? bytes - off : kGlaL2Piece;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char *>(p) + off),
+                 "r"((uint32_t)nb)
+                 : "memory");
+  }
+}
+
+// The state bytes of round r's heads (at most 64 KB from the round's start),
+// for the pipelined layout's first round.
+__device__ __forceinline__ void prefetch_first_round(const GlaParams &p, int es, int64_t r, int G) {
+  const int64_t h0 = r * G;
+  const int64_t nh = p.bh - h0 < G ? p.bh - h0 : G;
+  const int64_t hb = (int64_t)p.dk * p.dv * es;
+  const int64_t bytes = nh * hb < 4 * kGlaL2Piece ? nh * hb : 4 * kGlaL2Piece;
+  prefetch_l2_pieces(static_cast<const char *>(p.S) + h0 * hb, bytes, threadIdx.x & 31);
+}
+
 template <class T, int RIF>
 __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
   using IO = GlaIo<T>;
@@ -137,12 +164,14 @@ __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
   // Launched as a programmatic dependent launch: let the next kernel be
   // scheduled early, and touch no memory before the previous one is done --
   // except, with GLA_PREFETCH_STATE, the first state rows of the first
-  // round, which the caller promised no work in flight writes.
+  // round, which the caller promised no work in flight writes.  (An L2
+  // prefetch of them before the wait, as the pipelined layout makes,
+  // measured 1-8 % slower here.)
   allow_dependents();
+  const int64_t rounds = (p.bh + G - 1) / G;
   bool waited = p.early_state == 0;
   if (waited) wait_for_predecessor();
   const int cc = tl % cpr, rl = tl / cpr;
-  const int64_t rounds = (p.bh + G - 1) / G;
 
   for (int64_t r = blockIdx.x; r < rounds; r += gridDim.x) {
     const int64_t h0 = r * G;                    // first head of this round
@@ -226,6 +255,157 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_kernel(GlaParams p) {
 template <class T>
 __global__ void __launch_bounds__(kGlaThreads, 3) gla_decode_kernel_small(GlaParams p) {
   gla_decode_body<T, kGlaRowsInFlightSmall>(p);
+}
+
+// ---------------------------------------------------------------- pipelined
+// The CTA layout with the next round staged by asynchronous copies
+// (cp.async, 16 bytes each) into a second shared-memory buffer while the
+// current round computes, so that a CTA's loads never wait for its round
+// barriers.  For rounds of at most kGlaPipeRoundChunks 16-byte state chunks
+// with q, k, gk and v rows that are whole 16-byte chunks.
+//
+// Shared memory, per buffer b in {0, 1}: the round's state, as in global
+// memory ([G][dk][cpr] chunks: each thread copies exactly the chunks it will
+// read, so its own wait makes them visible), then q, k, gk ([G][dk] each,
+// QC chunks apart) and v ([G][dv]) in the input type, copied by all threads
+// and read by all after a barrier; then o's row-block partials [G][RP][dv].
+// The thread mapping, the fmaf per element and the order of every sum are
+// those of gla_decode_kernel with the same G: S_new is bit-identical, and o
+// too where the two choose the same G (G sets the row blocks o is summed in).
+// Before waiting on the preceding kernel, warp 0 asks L2 for the first
+// round's state (or, with GLA_PREFETCH_STATE, every thread already copies
+// its part of it): measured 3-8 % faster back to back.
+constexpr int kGlaPipeRoundChunks = 2048;
+// Shared memory of one CTA at most: three CTAs per SM (228 KB, 1 KB reserved
+// per CTA).
+constexpr int64_t kGlaPipeMaxSmem = 75 * 1024;
+
+int64_t gla_pipe_smem(int G, int64_t dk, int64_t dv, int cpr, int es) {
+  const int RP = (kGlaThreads / G) / cpr;
+  const int64_t buf = (int64_t)G * dk * cpr + 3 * ((int64_t)G * dk * es / 16) + (int64_t)G * cpr;
+  return 2 * buf * 16 + (int64_t)G * RP * dv * (int64_t)sizeof(float);
+}
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most one committed group of this thread is still pending.
+__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <class T>
+__global__ void __launch_bounds__(kGlaThreads) gla_decode_pipe_kernel(GlaParams p) {
+  using IO = GlaIo<T>;
+  constexpr int VEC = IO::VEC;
+  constexpr int ES = 16 / VEC;  // element size in bytes
+  extern __shared__ uint4 gsm4[];
+  const int dk = p.dk, dv = p.dv, G = p.heads_per_cta;
+  const int cpr = dv / VEC;
+  const int TPG = kGlaThreads / G, RP = TPG / cpr;
+  const int SC = G * dk * cpr;        // state chunks per buffer
+  const int QC = G * dk * ES / 16;    // chunks of one of q, k, gk per buffer (dk * ES % 16 == 0)
+  const int BUF = SC + 3 * QC + G * cpr;
+  float *part = reinterpret_cast<float *>(gsm4 + 2 * BUF);
+  const int t = threadIdx.x;
+  const int gi = t / TPG, tl = t % TPG;
+  const int cc = tl % cpr, rl = tl / cpr;
+  const int64_t rounds = (p.bh + G - 1) / G;
+  const uint4 *Sg = reinterpret_cast<const uint4 *>(p.S);
+
+  // This thread's state chunks of round r into buffer b.
+  auto issue_state = [&](int64_t r, int b) {
+    const int64_t h0 = r * G;
+    const int nh = (p.bh - h0 < G) ? (int)(p.bh - h0) : G;
+    if (rl < RP && gi < nh) {
+      uint4 *dst = gsm4 + (size_t)b * BUF + (size_t)gi * dk * cpr + cc;
+      const uint4 *src = Sg + ((h0 + gi) * dk) * (int64_t)cpr + cc;
+      for (int i = rl; i < dk; i += RP) cp_async16(dst + (size_t)i * cpr, src + (int64_t)i * cpr);
+    }
+  };
+  // Round r's q, k, gk and v into buffer b, dealt over all threads.
+  auto issue_vectors = [&](int64_t r, int b) {
+    const int64_t h0 = r * G;
+    const int nh = (p.bh - h0 < G) ? (int)(p.bh - h0) : G;
+    const int nq = nh * dk * ES / 16, nv = nh * cpr;
+    uint4 *base = gsm4 + (size_t)b * BUF + SC;
+    const int64_t q0 = h0 * dk * ES / 16;
+    for (int x = t; x < 3 * nq + nv; x += kGlaThreads) {
+      if (x < 3 * nq) {
+        const int a = x / nq, y = x % nq;
+        const void *v = a == 0 ? p.q : a == 1 ? p.k : p.gk;
+        cp_async16(base + a * QC + y, reinterpret_cast<const uint4 *>(v) + q0 + y);
+      } else {
+        const int y = x - 3 * nq;
+        cp_async16(base + 3 * QC + y, reinterpret_cast<const uint4 *>(p.v) + h0 * cpr + y);
+      }
+    }
+  };
+
+  allow_dependents();
+  int64_t r = blockIdx.x;
+  if (r >= rounds) {
+    wait_for_predecessor();
+    return;
+  }
+  // Launched as a programmatic dependent launch: with GLA_PREFETCH_STATE the
+  // first round's state is requested before waiting for the preceding
+  // kernel; without it, warp 0 only asks L2 for it.
+  if (p.early_state) {
+    issue_state(r, 0);
+    wait_for_predecessor();
+  } else {
+    if (t < 32) prefetch_first_round(p, ES, r, G);
+    wait_for_predecessor();
+    issue_state(r, 0);
+  }
+  issue_vectors(r, 0);
+  cp_async_commit();
+  for (int b = 0; r < rounds; r += gridDim.x, b ^= 1) {
+    const int64_t rn = r + gridDim.x;
+    if (rn < rounds) {  // buffer b ^ 1 was last read before the previous round's second barrier
+      issue_state(rn, b ^ 1);
+      issue_vectors(rn, b ^ 1);
+    }
+    cp_async_commit();
+    cp_async_wait_all_but_one();  // this thread's copies of round r have landed
+    __syncthreads();              // and everyone's (q, k, gk, v are shared)
+    const int64_t h0 = r * G;
+    const int nh = (p.bh - h0 < G) ? (int)(p.bh - h0) : G;
+    if (rl < RP && gi < nh) {
+      const int64_t h = h0 + gi;
+      const uint4 *buf = gsm4 + (size_t)b * BUF;
+      const uint4 *st = buf + (size_t)gi * dk * cpr + cc;
+      const void *qs = buf + SC, *ks = buf + SC + QC, *gs = buf + SC + 2 * QC;
+      float vv[VEC], acc[VEC];
+      IO::unpack(buf[SC + 3 * QC + gi * cpr + cc], vv);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+      uint4 *Nrow = reinterpret_cast<uint4 *>(p.S_new) + (h * dk) * (int64_t)cpr + cc;
+      for (int i = rl; i < dk; i += RP) {
+        float s[VEC], sn[VEC];
+        IO::unpack(st[(size_t)i * cpr], s);
+        const int x = gi * dk + i;
+        const float di = expf(IO::scalar(gs, x)), ki = IO::scalar(ks, x), qi = IO::scalar(qs, x);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          sn[e] = fmaf(di, s[e], ki * vv[e]);
+          acc[e] = fmaf(qi, sn[e], acc[e]);
+        }
+        stg_stream(Nrow + (int64_t)i * cpr, IO::pack(sn));
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) part[(gi * RP + rl) * dv + cc * VEC + e] = acc[e];
+    }
+    __syncthreads();
+    for (int x = t; x < nh * dv; x += kGlaThreads) {
+      const int g = x / dv, j = x % dv;
+      float sum = 0.f;
+      for (int rb = 0; rb < RP; ++rb) sum += part[(g * RP + rb) * dv + j];
+      IO::store_scalar(p.o, h0 * dv + x, p.scale * sum);
+    }
+  }
 }
 
 // One warp per head, for many small heads (dv * element size <= 512 bytes):
@@ -317,6 +497,21 @@ cudaError_t pdl_launch(const void *fn, unsigned grid, size_t smem, cudaStream_t 
   return e;
 }
 
+// Grid for `units` rounds of work dealt round-robin over at most `cap`
+// resident CTAs.  The fewest rounds per CTA the cap allows, then the fewest
+// CTAs that still finish in that many rounds, so that no CTA starts a last
+// round that most others skip (2048 heads over 608 slots: 512 CTAs of 4
+// rounds, not 608 CTAs of which 224 run a fourth) -- unless that drops more
+// than a fifth of the cap: each CTA round is latency-bound, and fewer CTAs
+// then cost more bandwidth than the ragged last round (measured on GB300 back
+// to back: 1-3 % faster at 84-96 % of the cap, 1-3 % slower at 75 %).
+int64_t balanced_grid(int64_t units, int64_t cap) {
+  if (units <= cap) return units;
+  const int64_t per = (units + cap - 1) / cap;
+  const int64_t grid = (units + per - 1) / per;
+  return 5 * grid >= 4 * cap ? grid : cap;
+}
+
 bool overlap_bytes(const void *p, int64_t pb, const void *q, int64_t qb) {
   const uintptr_t a0 = (uintptr_t)p, a1 = a0 + (uintptr_t)pb;
   const uintptr_t b0 = (uintptr_t)q, b1 = b0 + (uintptr_t)qb;
@@ -333,7 +528,7 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
                              int variant, int flags, cudaStream_t stream) {
   if (dtype != GLA_F16 && dtype != GLA_BF16 && dtype != GLA_F32) return GEMV_ERR_DTYPE;
   if (flags & ~GLA_PREFETCH_STATE) return GEMV_ERR_ARG;
-  if (variant < GLA_VARIANT_AUTO || variant > GLA_VARIANT_WARP) return GEMV_ERR_CONFIG;
+  if (variant < GLA_VARIANT_AUTO || variant > GLA_VARIANT_PIPE) return GEMV_ERR_CONFIG;
   if (bh < 0 || dk < 0 || dv < 0 || dk > kGlaMaxDk) return GEMV_ERR_ARG;
   if (bh == 0 || dv == 0) return GEMV_OK;
   const int es = dtype == GLA_F32 ? 4 : 2;
@@ -368,12 +563,21 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
   }
   if (major != 10 || minor != 3) return GEMV_ERR_DEVICE;
   const int cpr = (int)(dv / VEC);
+  // The pipelined CTA layout needs q, k, gk rows of whole 16-byte chunks and
+  // a round (G heads, G >= 1) of at most kGlaPipeRoundChunks state chunks.
+  const bool pipe_ok = dk > 0 && (dk * es) % 16 == 0 && ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)gk) & 15u) == 0) &&
+                       dk * cpr <= kGlaPipeRoundChunks && gla_pipe_smem(1, dk, dv, cpr, es) <= kGlaPipeMaxSmem;
   // The CTA layout with several heads per round measured faster than a
   // warp per head on every workload tried (4096 x 64 x 64 fp16: 18.5 vs
   // 20.5 us; 16384 x 16 x 64 fp16: 20.5 vs 28.7 us; 4096 x 128 x 128 bf16:
-  // 48.5 vs 61.2 us), so it is the automatic choice.
-  if (variant == GLA_VARIANT_AUTO) variant = GLA_VARIANT_CTA;
+  // 48.5 vs 61.2 us).  Its pipelined form measured 1 % faster for heads of
+  // more than kGlaSmallHeadChunks chunks (128 x 128 bf16) and 2-10 % slower
+  // for smaller ones (64 x 64, 16 x 64: half the heads per round within
+  // its shared memory), so it is chosen for the former only.
+  if (variant == GLA_VARIANT_AUTO)
+    variant = pipe_ok && (int64_t)dk * cpr > kGlaSmallHeadChunks ? GLA_VARIANT_PIPE : GLA_VARIANT_CTA;
   if (variant == GLA_VARIANT_WARP && cpr > 32) return GEMV_ERR_CONFIG;
+  if (variant == GLA_VARIANT_PIPE && !pipe_ok) return GEMV_ERR_CONFIG;
   GlaParams p;
   p.q = q; p.k = k; p.v = v; p.gk = gk; p.S = S; p.S_new = S_new; p.o = o;
   p.bh = bh; p.dk = (int32_t)dk; p.dv = (int32_t)dv; p.scale = scale; p.heads_per_cta = 1;
@@ -388,9 +592,34 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
       return GEMV_ERR_CONFIG;
     }
     const int64_t warps = kGlaThreads / 32;
-    int64_t grid = (int64_t)sms * per_sm;
-    if (grid > (bh + warps - 1) / warps) grid = (bh + warps - 1) / warps;
+    const int64_t grid = (balanced_grid(bh, (int64_t)sms * per_sm * warps) + warps - 1) / warps;
     if (pdl_launch((const void *)fw, (unsigned)grid, 0, stream, p) != cudaSuccess) return GEMV_ERR_CUDA;
+    return GEMV_OK;
+  }
+  if (variant == GLA_VARIANT_PIPE) {
+    // Heads per round: as many as keep a round within kGlaPipeRoundChunks
+    // chunks, the buffers within kGlaPipeMaxSmem, and at least one row block
+    // of cpr threads per head.
+    int G = 1;
+    while (2 * G * cpr <= kGlaThreads && (int64_t)2 * G <= bh && (int64_t)dk * cpr * (2 * G) <= kGlaPipeRoundChunks &&
+           gla_pipe_smem(2 * G, dk, dv, cpr, es) <= kGlaPipeMaxSmem)
+      G *= 2;
+    p.heads_per_cta = G;
+    const size_t smem = (size_t)gla_pipe_smem(G, dk, dv, cpr, es);
+    void (*fn)(GlaParams) = dtype == GLA_F16 ? gla_decode_pipe_kernel<F16>
+                            : dtype == GLA_BF16 ? gla_decode_pipe_kernel<BF16> : gla_decode_pipe_kernel<F32>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute((const void *)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return GEMV_ERR_CUDA;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)fn, kGlaThreads, smem) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      return GEMV_ERR_CONFIG;
+    }
+    const int64_t grid = balanced_grid((bh + G - 1) / G, (int64_t)sms * per_sm);
+    if (pdl_launch((const void *)fn, (unsigned)grid, smem, stream, p) != cudaSuccess) return GEMV_ERR_CUDA;
     return GEMV_OK;
   }
   // Rows in flight per thread, and heads side by side per CTA round: enough
@@ -422,9 +651,7 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
     cudaGetLastError();
     return GEMV_ERR_CONFIG;
   }
-  int64_t grid = (int64_t)sms * per_sm;
-  const int64_t rounds = (bh + G - 1) / G;
-  if (grid > rounds) grid = rounds;
+  const int64_t grid = balanced_grid((bh + G - 1) / G, (int64_t)sms * per_sm);
   if (pdl_launch((const void *)fn, (unsigned)grid, smem, stream, p) != cudaSuccess) return GEMV_ERR_CUDA;
   return GEMV_OK;
 }

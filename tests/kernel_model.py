@@ -350,6 +350,17 @@ def staged_shifted(a, j0, seglen, off, as_elems):
 
 
 
+def gla_balanced_grid(units, cap):
+    """The host's grid for `units` rounds dealt round-robin over at most
+    `cap` resident CTAs: the fewest rounds per CTA, then the fewest CTAs --
+    unless that is below 4/5 of the cap, which then stays."""
+    if units <= cap:
+        return units
+    per = -(-units // cap)
+    grid = -(-units // per)
+    return grid if 5 * grid >= 4 * cap else cap
+
+
 def gla_rows_in_flight(dk, cpr):
     """The host's choice of rows in flight per thread: 8 for heads of at most
     1024 16-byte chunks, else 4."""
@@ -417,6 +428,148 @@ def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=None, grid=No
                 o_written[h0 + g, j] += 1
     assert (touched == 1).all() and (o_written == 1).all()
     return {"smem_floats": smem_floats, "heads_per_cta": G}
+
+
+GLA_PIPE_ROUND_CHUNKS = 2048
+
+
+GLA_PIPE_MAX_SMEM = 75 * 1024
+
+
+def gla_pipe_smem(G, dk, dv, elem_bytes, threads=256):
+    cpr = dv * elem_bytes // 16
+    RP = threads // G // cpr
+    return 2 * 16 * (G * dk * cpr + 3 * (G * dk * elem_bytes // 16) + G * cpr) + 4 * G * RP * dv
+
+
+def gla_pipe_ok(dk, dv, elem_bytes):
+    """The host's condition for the pipelined layout (aligned pointers
+    assumed): q, k, gk rows of whole 16-byte chunks, one head within a round
+    and its buffers within the shared-memory budget."""
+    cpr = dv * elem_bytes // 16
+    return (dk > 0 and (dk * elem_bytes) % 16 == 0 and dk * cpr <= GLA_PIPE_ROUND_CHUNKS
+            and gla_pipe_smem(1, dk, dv, elem_bytes) <= GLA_PIPE_MAX_SMEM)
+
+
+def gla_auto_is_pipe(dk, dv, elem_bytes):
+    """The automatic choice (aligned pointers assumed): the pipelined layout
+    for heads of more than 1024 16-byte chunks where it applies, else the
+    CTA layout."""
+    return gla_pipe_ok(dk, dv, elem_bytes) and dk * (dv * elem_bytes // 16) > 1024
+
+
+def gla_pipe_heads_per_cta(bh, dk, dv, elem_bytes, threads=256):
+    cpr = dv * elem_bytes // 16
+    G = 1
+    while (2 * G * cpr <= threads and 2 * G <= bh and dk * cpr * 2 * G <= GLA_PIPE_ROUND_CHUNKS
+           and gla_pipe_smem(2 * G, dk, dv, elem_bytes, threads) <= GLA_PIPE_MAX_SMEM):
+        G *= 2
+    return G
+
+
+def replay_gla_pipe(bh, dk, dv, elem_bytes, threads=256, grid=None):
+    """Index replay of ``gla_decode_pipe_kernel``: per CTA, round r's copies
+    go to buffer j % 2 (j = the CTA's round count so far) -- every state
+    chunk copied once, by the thread that later reads it, from inside S into
+    inside its buffer; q, k, gk, v chunks copied once per round from inside
+    their arrays; every staged element read by the compute was copied for
+    that round into that buffer; no copy targets the buffer a round still
+    reads; partials and o as in the CTA layout; the shared-memory size is
+    the host's."""
+    vec = 16 // elem_bytes
+    cpr = dv // vec
+    assert gla_pipe_ok(dk, dv, elem_bytes) and 1 <= cpr <= threads
+    G = gla_pipe_heads_per_cta(bh, dk, dv, elem_bytes, threads)
+    TPG = threads // G
+    RP = TPG // cpr
+    assert RP >= 1 and G * dk * cpr <= GLA_PIPE_ROUND_CHUNKS
+    SC, QC = G * dk * cpr, G * dk * elem_bytes // 16
+    BUF = SC + 3 * QC + G * cpr
+    smem = 2 * BUF * 16 + G * RP * dv * 4
+    assert smem == gla_pipe_smem(G, dk, dv, elem_bytes, threads) <= GLA_PIPE_MAX_SMEM
+    rounds = -(-bh // G)
+    grid = rounds if grid is None else min(grid, rounds)
+    s_chunks, q_chunks, v_chunks = bh * dk * cpr, bh * dk * elem_bytes // 16, bh * cpr
+    read = np.zeros(s_chunks, dtype=np.int32)
+    vec_copied = np.zeros((3, q_chunks), dtype=np.int32)
+    v_copied = np.zeros(v_chunks, dtype=np.int32)
+    o_written = np.zeros((bh, dv), dtype=np.int32)
+
+    def copies(r, b):
+        """{(smem chunk): (kind, global chunk, thread)} of round r into buffer b."""
+        out = {}
+        h0 = r * G
+        nh = min(G, bh - h0)
+        for t in range(threads):
+            gi, tl = divmod(t, TPG)
+            cc, rl = tl % cpr, tl // cpr
+            if rl < RP and gi < nh:
+                for i in range(rl, dk, RP):
+                    dst = b * BUF + (gi * dk + i) * cpr + cc
+                    src = ((h0 + gi) * dk + i) * cpr + cc
+                    assert dst not in out and 0 <= src < s_chunks
+                    out[dst] = ("S", src, t)
+        nq, nv = nh * dk * elem_bytes // 16, nh * cpr
+        q0 = h0 * dk * elem_bytes // 16
+        for t in range(threads):
+            for x in range(t, 3 * nq + nv, threads):
+                if x < 3 * nq:
+                    a, y = divmod(x, nq)
+                    dst, src = b * BUF + SC + a * QC + y, q0 + y
+                    assert 0 <= src < q_chunks and y < QC
+                    out[dst] = ("qkg"[a], src, t)
+                else:
+                    y = x - 3 * nq
+                    dst, src = b * BUF + SC + 3 * QC + y, h0 * cpr + y
+                    assert 0 <= src < v_chunks and y < G * cpr
+                    out[dst] = ("v", src, t)
+        for dst in out:
+            assert b * BUF <= dst < (b + 1) * BUF
+        return out
+
+    for blk in range(grid):
+        my = list(range(blk, rounds, grid))
+        pending = {0: copies(my[0], 0)} if my else {}
+        for j, r in enumerate(my):
+            b = j % 2
+            if j + 1 < len(my):
+                nxt = copies(my[j + 1], b ^ 1)
+                assert all(d // BUF == b ^ 1 for d in nxt)  # never the buffer round j reads
+                pending[b ^ 1] = nxt
+            cur = pending.pop(b)
+            for kind, src, _ in cur.values():
+                if kind in "qkg":
+                    vec_copied["qkg".index(kind), src] += 1
+                elif kind == "v":
+                    v_copied[src] += 1
+            h0 = r * G
+            nh = min(G, bh - h0)
+            for t in range(threads):
+                gi, tl = divmod(t, TPG)
+                cc, rl = tl % cpr, tl // cpr
+                if not (rl < RP and gi < nh):
+                    continue
+                h = h0 + gi
+                vsm = b * BUF + SC + 3 * QC + gi * cpr + cc
+                assert cur[vsm][0] == "v" and cur[vsm][1] == h * cpr + cc
+                for i in range(rl, dk, RP):
+                    sm = b * BUF + (gi * dk + i) * cpr + cc
+                    kind, src, owner = cur[sm]
+                    assert kind == "S" and owner == t and src == (h * dk + i) * cpr + cc
+                    read[src] += 1
+                    x = gi * dk + i  # element of q, k, gk in the buffer
+                    for a in range(3):
+                        qsm = b * BUF + SC + a * QC + (x * elem_bytes) // 16
+                        assert cur[qsm][0] == "qkg"[a]
+                        assert cur[qsm][1] * 16 // elem_bytes + (x * elem_bytes % 16) // elem_bytes == h * dk + i
+                base = 2 * BUF * 16 + ((gi * RP + rl) * dv + cc * vec) * 4
+                assert base + 4 * vec <= smem
+            for x in range(nh * dv):
+                g, jj = divmod(x, dv)
+                o_written[h0 + g, jj] += 1
+    assert (read == 1).all() and (o_written == 1).all()
+    assert (vec_copied == 1).all() and (v_copied == 1).all()
+    return {"smem_bytes": smem, "heads_per_cta": G}
 
 
 def replay_gla_warp(bh, dk, dv, elem_bytes, warps_per_cta=8, grid=None, rows_in_flight=8):

@@ -105,13 +105,16 @@ def test_gla_fuzz(cuda_dev, case):
     bh = int(rng.choice([1, 3, 17, 64, 300]))
     dk = int(rng.choice([0, 1, 5, 16, 64, 100, 128, 256]))
     dv = vec * int(rng.choice([1, 2, 3, 5, 8, 16, 32]))
-    variant = int(rng.choice([0, 1, 2]))
+    variant = int(rng.choice([0, 1, 2, 3]))
     in_place = bool(rng.integers(2))
     warp_ok = dv * es <= 512
-    if variant == 2 and not warp_ok:
+    pipe_ok = kernel_model.gla_pipe_ok(dk, dv, es)
+    if (variant == 2 and not warp_ok) or (variant == 3 and not pipe_ok):
         variant = 1
     if variant == 2:
         kernel_model.replay_gla_warp(bh, dk, dv, es, grid=None)
+    elif variant == 3 or (variant == 0 and kernel_model.gla_auto_is_pipe(dk, dv, es)):
+        kernel_model.replay_gla_pipe(bh, dk, dv, es)
     else:
         kernel_model.replay_gla(bh, dk, dv, es)
     gen = torch.Generator(device=cuda_dev)

@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import kernel_model
 import memory_bound_gemv_02_gb300 as g
 import oracle
 import parity_rules
@@ -74,13 +75,30 @@ def _warp_ok(dv, dtype):
     return dv * (4 if dtype == torch.float32 else 2) <= 512
 
 
+def _pipe_ok(dk, dv, dtype):
+    """The pipelined layout's shape condition (pointers 16-byte aligned)."""
+    return kernel_model.gla_pipe_ok(dk, dv, 4 if dtype == torch.float32 else 2)
+
+
+def _variant_ok(variant, dk, dv, dtype):
+    if variant == g.GLA_VARIANT_WARP:
+        return _warp_ok(dv, dtype)
+    if variant == g.GLA_VARIANT_PIPE:
+        return _pipe_ok(dk, dv, dtype)
+    return True
+
+
+ALL = [g.GLA_VARIANT_AUTO, g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP, g.GLA_VARIANT_PIPE]
+FORCED = [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP, g.GLA_VARIANT_PIPE]
+
+
 @pytest.mark.parametrize("bh,dk,dv", SHAPES + [(40, 64, 64), (9, 33, 256), (37, 16, 64), (11, 5, 24), (300, 8, 64)])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("variant", [g.GLA_VARIANT_AUTO, g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+@pytest.mark.parametrize("variant", ALL)
 def test_gla_parity(cuda_dev, bh, dk, dv, dtype, variant):
     if dtype == torch.float32 and dv // 4 > 256:
         pytest.skip("dv / 4 > 256 is outside the kernel's range for fp32")
-    if variant == g.GLA_VARIANT_WARP and not _warp_ok(dv, dtype):
+    if not _variant_ok(variant, dk, dv, dtype):
         with pytest.raises(g.GemvError) as ei:
             q, k, v, gk, S = _make(bh, dk, dv, dtype, 1, cuda_dev)
             g.gla_decode(q, k, v, gk, S, scale=1.0, variant=variant)
@@ -94,9 +112,10 @@ def test_gla_parity(cuda_dev, bh, dk, dv, dtype, variant):
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("variant", [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+@pytest.mark.parametrize("variant", FORCED)
 def test_gla_in_place(cuda_dev, dtype, variant):
-    q, k, v, gk, S = _make(16, 128, 128, dtype, 5, cuda_dev)
+    d = 64 if dtype == torch.float32 else 128  # a shape every layout takes
+    q, k, v, gk, S = _make(16, d, d, dtype, 5, cuda_dev)
     S_in = S.clone()
     S_new, o = g.gla_decode(q, k, v, gk, S, scale=0.125, S_new=S, variant=variant)
     assert S_new.data_ptr() == S.data_ptr()
@@ -106,23 +125,64 @@ def test_gla_in_place(cuda_dev, dtype, variant):
 @pytest.mark.parametrize("bh,dk,dv,dtype", [(4096, 64, 64, torch.float16), (2600, 128, 128, torch.bfloat16),
                                             (3000, 16, 128, torch.float32), (5, 200, 40, torch.float16)])
 def test_gla_layouts_agree(cuda_dev, bh, dk, dv, dtype):
-    """The two layouts store bit-identical states (same fmaf per element) and
-    o within the sum-order tolerance; the automatic choice is the CTA
-    layout."""
+    """The layouts store bit-identical states (same fmaf per element) and o
+    within the sum-order tolerance; the automatic choice is the pipelined
+    layout for large heads where it applies, else the CTA layout."""
     q, k, v, gk, S = _make(bh, dk, dv, dtype, 21, cuda_dev)
     S_c, o_c = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_CTA)
     S_w, o_w = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_WARP)
+    outs = {"cta": (S_c, o_c), "warp": (S_w, o_w)}
+    pipe = _pipe_ok(dk, dv, dtype)
+    if pipe:
+        outs["pipe"] = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_PIPE)
     torch.cuda.synchronize()
-    assert torch.equal(_t(S_c), _t(S_w))
-    if bh <= 64:
-        _check(q, k, v, gk, S, S_w, o_w, 0.25, "warp layout")
-    else:
-        rows = torch.arange(0, bh, max(1, bh // 40), device=cuda_dev)
-        _check(q[rows], k[rows], v[rows], gk[rows], S[rows], S_w[rows], o_w[rows], 0.25, "warp layout sampled")
-        _check(q[rows], k[rows], v[rows], gk[rows], S[rows], S_c[rows], o_c[rows], 0.25, "cta layout sampled")
+    for name, (S_x, o_x) in outs.items():
+        assert torch.equal(_t(S_c), _t(S_x)), name
+        if bh <= 64:
+            _check(q, k, v, gk, S, S_x, o_x, 0.25, f"{name} layout")
+        else:
+            rows = torch.arange(0, bh, max(1, bh // 40), device=cuda_dev)
+            _check(q[rows], k[rows], v[rows], gk[rows], S[rows], S_x[rows], o_x[rows], 0.25, f"{name} sampled")
     S_a, o_a = g.gla_decode(q, k, v, gk, S, scale=0.25)
     torch.cuda.synchronize()
-    assert torch.equal(_t(o_a), _t(o_c)) and torch.equal(_t(S_a), _t(S_c))
+    want = outs["pipe" if kernel_model.gla_auto_is_pipe(dk, dv, 4 if dtype == torch.float32 else 2) else "cta"]
+    assert torch.equal(_t(o_a), _t(want[1])) and torch.equal(_t(S_a), _t(want[0]))
+
+
+@pytest.mark.parametrize("bh,dk,dv,dtype", [(2048, 128, 128, torch.bfloat16), (300, 64, 128, torch.float32),
+                                            (37, 32, 256, torch.float16), (1000, 8, 16, torch.bfloat16)])
+def test_gla_pipe_same_heads_per_round_bit_identical(cuda_dev, bh, dk, dv, dtype):
+    """Where the pipelined and the CTA layouts take the same heads per round
+    (G), they sum o in the same row blocks in the same order: both outputs
+    are bit-identical."""
+    es = 4 if dtype == torch.float32 else 2
+    cpr = dv * es // 16
+    G_pipe = kernel_model.gla_pipe_heads_per_cta(bh, dk, dv, es)
+    G_cta = kernel_model.gla_heads_per_cta(bh, dk, cpr)
+    if G_pipe != G_cta:
+        pytest.skip(f"heads per round differ ({G_pipe} vs {G_cta})")
+    q, k, v, gk, S = _make(bh, dk, dv, dtype, 23, cuda_dev)
+    S_c, o_c = g.gla_decode(q, k, v, gk, S, scale=0.3, variant=g.GLA_VARIANT_CTA)
+    S_p, o_p = g.gla_decode(q, k, v, gk, S, scale=0.3, variant=g.GLA_VARIANT_PIPE)
+    torch.cuda.synchronize()
+    assert torch.equal(_t(S_c), _t(S_p)) and torch.equal(_t(o_c), _t(o_p))
+
+
+def test_gla_pipe_alignment_fallback(cuda_dev):
+    """q one element off a 16-byte boundary: the automatic choice falls back
+    to the CTA layout (same results), the pipelined layout refuses."""
+    bh, dk, dv = 64, 64, 64
+    q, k, v, gk, S = _make(bh, dk, dv, torch.float16, 24, cuda_dev)
+    qbuf = torch.empty(bh * dk + 1, dtype=torch.float16, device=cuda_dev)
+    qbuf[1:].copy_(q.reshape(-1))
+    q_off = qbuf[1:].view(bh, dk)
+    S_a, o_a = g.gla_decode(q_off, k, v, gk, S, scale=0.2)
+    S_c, o_c = g.gla_decode(q, k, v, gk, S, scale=0.2, variant=g.GLA_VARIANT_CTA)
+    torch.cuda.synchronize()
+    assert torch.equal(_t(S_a), _t(S_c)) and torch.equal(_t(o_a), _t(o_c))
+    with pytest.raises(g.GemvError) as ei:
+        g.gla_decode(q_off, k, v, gk, S, scale=0.2, variant=g.GLA_VARIANT_PIPE)
+    assert ei.value.status == g.GEMV_ERR_CONFIG
 
 
 def _t(x):
@@ -130,7 +190,7 @@ def _t(x):
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("variant", [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+@pytest.mark.parametrize("variant", FORCED)
 def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype, variant):
     """gk = 0 and small integers: every fp32 operation is exact, so the stored
     state and o equal the oracle rounded once."""
@@ -148,7 +208,7 @@ def test_gla_integer_inputs_no_decay_exact(cuda_dev, dtype, variant):
     assert (_bits(o) == oracle.encode(ref_o, fmt)).all()
 
 
-@pytest.mark.parametrize("variant", [g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+@pytest.mark.parametrize("variant", FORCED)
 def test_gla_multiple_steps_match_stepwise_oracle(cuda_dev, variant):
     """Ten chained decode steps on one state (in place), each checked."""
     bh, dk, dv = 12, 64, 64
@@ -183,7 +243,7 @@ def test_gla_empty_dk_and_errors(cuda_dev):
     assert ei.value.status == g.GEMV_ERR_ALIAS
 
 
-@pytest.mark.parametrize("variant", [g.GLA_VARIANT_AUTO, g.GLA_VARIANT_CTA, g.GLA_VARIANT_WARP])
+@pytest.mark.parametrize("variant", ALL)
 @pytest.mark.parametrize("bh,d,dtype", [(64, 64, torch.bfloat16), (300, 128, torch.float16), (48, 32, torch.float32)])
 def test_gla_prefetch_state_layer_chain(cuda_dev, variant, bh, d, dtype):
     """GLA_PREFETCH_STATE over a stack of layers, each owning its state: step

@@ -223,6 +223,61 @@ def test_gla_index_replay(bh, dk, dv, es, grid):
     kernel_model.replay_gla(bh, dk, dv, es, grid=grid)
 
 
+def test_gla_balanced_grid():
+    """The GLA grid: never above the resident cap, every CTA gets a round,
+    no CTA runs more rounds than the cap forces (ceil(units / cap)), the
+    round counts differ by at most one, and it stays at the cap when
+    balancing would drop more than a fifth of it."""
+    bg = kernel_model.gla_balanced_grid
+    assert bg(2048, 608) == 512 and bg(4096, 608) == 586 and bg(2048, 456) == 410 and bg(100, 608) == 100
+    assert bg(1024, 456) == 456 and bg(1024, 608) == 512
+    for units in list(range(1, 400)) + [2047, 2048, 2049, 4096, 65536, 10**6 + 7]:
+        for cap in (1, 3, 152, 304, 456, 608, 1216):
+            grid = bg(units, cap)
+            assert 1 <= grid <= min(units, cap)
+            assert grid == min(units, cap) or 5 * grid >= 4 * cap
+            per = [len(range(b, units, grid)) for b in range(grid)] if units < 5000 else None
+            if per is not None:
+                assert min(per) >= 1 and max(per) == -(-units // cap) and max(per) - min(per) <= 1
+
+
+@pytest.mark.parametrize("bh,dk,dv,es,cap", [(2048, 8, 64, 2, 608), (1031, 3, 16, 4, 152), (300, 16, 64, 2, 456)])
+def test_gla_index_replay_balanced_grid(bh, dk, dv, es, cap):
+    """The replay at the grid the host computes from a resident cap."""
+    cpr = dv * es // 16
+    G = kernel_model.gla_heads_per_cta(bh, dk, cpr)
+    kernel_model.replay_gla(bh, dk, dv, es, grid=kernel_model.gla_balanced_grid(-(-bh // G), cap))
+    kernel_model.replay_gla_warp(bh, dk, dv, es, grid=-(-kernel_model.gla_balanced_grid(bh, cap * 8) // 8))
+
+
+@pytest.mark.parametrize("bh,dk,dv,es", [(3, 128, 128, 2), (2, 64, 64, 4), (5, 16, 8, 2), (9, 8, 256, 2),
+                                         (2, 64, 128, 4), (4, 16, 24, 2), (7, 64, 64, 2), (37, 16, 64, 2),
+                                         (11, 8, 24, 2), (6, 4, 40, 4), (300, 16, 64, 2), (1, 200, 64, 2)])
+@pytest.mark.parametrize("grid", [1, 3, None])
+def test_gla_pipe_index_replay(bh, dk, dv, es, grid):
+    kernel_model.replay_gla_pipe(bh, dk, dv, es, grid=grid)
+
+
+def test_gla_pipe_choice():
+    """The pipelined layout applies to rows of whole 16-byte chunks and
+    heads within 32 KiB; the workload shapes 2048 x 128 x 128 bf16, 4096 x
+    64 x 64 fp16 and 16384 x 16 x 64 fp16 take it with 1, 2 and 8 heads
+    per round, in buffers of which 3 CTAs fit an SM (228 KB, 1 KB reserved
+    per CTA)."""
+    ok, hp = kernel_model.gla_pipe_ok, kernel_model.gla_pipe_heads_per_cta
+    assert ok(128, 128, 2) and ok(64, 64, 2) and ok(16, 64, 2) and ok(64, 64, 4)
+    assert not ok(128, 128, 4) and not ok(256, 256, 2) and not ok(5, 64, 2) and not ok(0, 64, 2)
+    assert hp(2048, 128, 128, 2) == 1 and hp(4096, 64, 64, 2) == 2 and hp(16384, 16, 64, 2) == 8
+    assert hp(8192, 64, 64, 4) == 2
+    auto = kernel_model.gla_auto_is_pipe
+    assert auto(128, 128, 2) and not auto(64, 64, 2) and not auto(16, 64, 2) and not auto(128, 128, 4)
+    for bh, dk, dv, es in [(2048, 128, 128, 2), (4096, 64, 64, 2), (16384, 16, 64, 2), (2048, 64, 64, 4),
+                           (5, 8, 2048, 2), (64, 2048, 8, 2)]:
+        if ok(dk, dv, es):
+            smem = kernel_model.gla_pipe_smem(hp(bh, dk, dv, es), dk, dv, es)
+            assert 3 * (smem + 1024) <= 233472, (bh, dk, dv, smem)
+
+
 def test_gla_heads_per_cta_choice():
     """Small heads are processed several per CTA round (about 4 rows per
     thread), large ones one per round."""
