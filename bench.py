@@ -404,10 +404,12 @@ def native_host_overhead():
 
 
 def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, variant=0):
-    """One shape: µs per call three ways -- isolated (CUDA events around each
-    launch), back to back, and back to back with programmatic dependent
-    launch -- and the launch configuration.  ``variant``: a GEMV_VARIANT_*
-    forced on every call (0: the planner's choice)."""
+    """One shape: µs per call four ways -- isolated (CUDA events around each
+    launch), back to back, back to back as gemv() launches (programmatic
+    dependent launch, first tile prefetched into L2 before the wait), and
+    back to back with the first tile read before the wait (B promised
+    unwritten) -- and the launch configuration.  ``variant``: a
+    GEMV_VARIANT_* forced on every call (0: the planner's choice)."""
     import torch
 
     from memory_bound_gemv_02_gb300 import inputs
@@ -429,9 +431,14 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, var
     ov.variant = variant
     ov.overlap = g.GEMV_OVERLAP_PDL_PREFETCH_B
     pdl = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(ov), s)) for Bx in Bs]
+    dc = g.GemvConfig()
+    dc.variant = variant
+    dc.overlap = g.GEMV_OVERLAP_PDL
+    dflt = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(dc), s)) for Bx in Bs]
     _, per = time_calls(L, plain, s, steps, warmup)
     el_plain = time_batch(plain, steps, warmup)
     el_pdl = time_batch(pdl, steps, warmup)
+    el_dflt = time_batch(dflt, steps, warmup)
     iso = statistics.median(per) * 1e3
     b2b = el_plain / steps * 1e6
     b2b_pdl = el_pdl / steps * 1e6
@@ -441,6 +448,7 @@ def bench_shape(g, L, n, k, dtype, out_fp32, dist, seed, steps, warmup, dev, var
             "us_isolated_p90": round(sorted(per)[int(0.9 * (len(per) - 1))] * 1e3, 3),
             "stddev_over_median": round(statistics.pstdev(per) / statistics.median(per), 4),
             "us_back_to_back": round(b2b, 3), "us_back_to_back_pdl": round(b2b_pdl, 3),
+            "us_back_to_back_default": round(el_dflt / steps * 1e6, 3),
             "gbs_isolated": round(nbytes / iso / 1e3, 1), "gbs_back_to_back": round(nbytes / b2b / 1e3, 1),
             "gbs_back_to_back_pdl": round(nbytes / b2b_pdl / 1e3, 1),
             "config": {kk: cfg[kk] for kk in ("variant", "rows_per_warp", "unroll", "warps_per_cta",
@@ -481,7 +489,7 @@ def run_sweep(args, dev):
         rb = bench_shape(g, L, n, k, dtype, out_fp32, dist, 0, args.sweep_steps, 20, dev,
                          variant=g.GEMV_VARIANT_BULK)
         r["bulk"] = {kk: rb[kk] for kk in ("us_isolated_median", "us_back_to_back", "us_back_to_back_pdl",
-                                           "gbs_back_to_back_pdl", "config")}
+                                           "us_back_to_back_default", "gbs_back_to_back_pdl", "config")}
         # context only (never a target): torch.mv (cuBLAS) on the same shape and box
         r["torch_mv_us_back_to_back"] = round(torch_mv_us(n, k, dtype, out_fp32, dist, dev, args.sweep_steps), 3)
         out.write(json.dumps(r) + "\n")

@@ -104,6 +104,9 @@ struct GlaIo<F32> {
 };
 
 constexpr int kGlaThreads = 256;
+
+// Floats to add after x floats to reach a multiple of 4 (16 bytes).
+__host__ __device__ constexpr int gla_pad4(int64_t x) { return (int)((4 - (x & 3)) & 3); }
 constexpr int kGlaMaxDk = 4096;
 // Rows of 16-byte chunks in flight per thread in the CTA layout: 8 for heads
 // of at most kGlaSmallHeadChunks chunks (with registers capped for 3 CTAs
@@ -119,6 +122,30 @@ __device__ __forceinline__ void stg_stream(uint4 *p, const uint4 &v) {
   asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+
+// Store a thread's VEC partial sums of o at float offset `off` of `part`
+// (a multiple of 4) as 16-byte vectors.  With 8 per thread, neighbouring
+// lanes' offsets are 8 floats apart and lanes 4 apart would hit the same
+// bank group; those with bit 5 of the offset set store their second half
+// first, so that each group of 8 lanes writes 8 distinct bank groups.
+template <int VEC>
+__device__ __forceinline__ void store_partials(float *part, int off, const float (&acc)[VEC]) {
+  float4 *d = reinterpret_cast<float4 *>(part + off);
+  if constexpr (VEC == 4) {
+    d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  } else {
+    static_assert(VEC == 8, "16-byte chunks hold 4 or 8 elements");
+    const float4 lo = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    const float4 hi = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if ((off >> 5) & 1) {
+      d[1] = hi;
+      d[0] = lo;
+    } else {
+      d[0] = lo;
+      d[1] = hi;
+    }
+  }
 }
 
 // Ask L2 for bytes [p, p + min(bytes, 32 * 16 KB)), a multiple of 16, in
@@ -150,7 +177,7 @@ template <class T, int RIF>
 __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
   using IO = GlaIo<T>;
   constexpr int VEC = IO::VEC;
-  extern __shared__ float gsm[];
+  extern __shared__ __align__(16) float gsm[];
   const int dk = p.dk, dv = p.dv, G = p.heads_per_cta;
   const int cpr = dv / VEC;               // 16-byte chunks per row
   const int TPG = kGlaThreads / G;        // threads per head
@@ -158,7 +185,7 @@ __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
   float *dec = gsm;                       // exp(gk)   [G][dk]
   float *kk = dec + G * dk;               // k         [G][dk]
   float *qq = kk + G * dk;                // q         [G][dk]
-  float *part = qq + G * dk;              // row-block partials of o [G][RP][dv]
+  float *part = qq + G * dk + gla_pad4(3 * G * dk);  // row-block partials of o [G][RP][dv], 16-byte aligned
   const int t = threadIdx.x;
   const int gi = t / TPG, tl = t % TPG;   // head slot of this thread, its index in the slot
   // Launched as a programmatic dependent launch: let the next kernel be
@@ -230,8 +257,7 @@ __device__ __forceinline__ void gla_decode_body(const GlaParams &p) {
           }
         }
       }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) part[(gi * RP + rl) * dv + cc * VEC + e] = acc[e];
+      store_partials<VEC>(part, (gi * RP + rl) * dv + cc * VEC, acc);
     }
     __syncthreads();
     for (int x = t; x < nh * dv; x += kGlaThreads) {
@@ -395,8 +421,7 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_pipe_kernel(GlaParams 
         }
         stg_stream(Nrow + (int64_t)i * cpr, IO::pack(sn));
       }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) part[(gi * RP + rl) * dv + cc * VEC + e] = acc[e];
+      store_partials<VEC>(part, (gi * RP + rl) * dv + cc * VEC, acc);
     }
     __syncthreads();
     for (int x = t; x < nh * dv; x += kGlaThreads) {
@@ -568,14 +593,12 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
   const bool pipe_ok = dk > 0 && (dk * es) % 16 == 0 && ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)gk) & 15u) == 0) &&
                        dk * cpr <= kGlaPipeRoundChunks && gla_pipe_smem(1, dk, dv, cpr, es) <= kGlaPipeMaxSmem;
   // The CTA layout with several heads per round measured faster than a
-  // warp per head on every workload tried (4096 x 64 x 64 fp16: 18.5 vs
-  // 20.5 us; 16384 x 16 x 64 fp16: 20.5 vs 28.7 us; 4096 x 128 x 128 bf16:
-  // 48.5 vs 61.2 us).  Its pipelined form measured 1 % faster for heads of
-  // more than kGlaSmallHeadChunks chunks (128 x 128 bf16) and 2-10 % slower
-  // for smaller ones (64 x 64, 16 x 64: half the heads per round within
-  // its shared memory), so it is chosen for the former only.
-  if (variant == GLA_VARIANT_AUTO)
-    variant = pipe_ok && (int64_t)dk * cpr > kGlaSmallHeadChunks ? GLA_VARIANT_PIPE : GLA_VARIANT_CTA;
+  // warp per head on every workload tried (4096 x 64 x 64 fp16: 16.0 vs
+  // 18.2 us; 16384 x 16 x 64 fp16: 19.0 vs 27.0 us; 4096 x 128 x 128 bf16:
+  // 45.4 vs 53.6 us), and its pipelined form faster still on every
+  // workload it takes (2048 x 128 x 128 bf16: 23.1 vs 25.8 us; 8192 x 64 x
+  // 64 bf16: 24.6 vs 27.5 us; 16384 x 16 x 64 fp16: 16.7 vs 19.0 us).
+  if (variant == GLA_VARIANT_AUTO) variant = pipe_ok ? GLA_VARIANT_PIPE : GLA_VARIANT_CTA;
   if (variant == GLA_VARIANT_WARP && cpr > 32) return GEMV_ERR_CONFIG;
   if (variant == GLA_VARIANT_PIPE && !pipe_ok) return GEMV_ERR_CONFIG;
   GlaParams p;
@@ -633,7 +656,8 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
     G *= 2;
   p.heads_per_cta = G;
   const int RP = (kGlaThreads / G) / cpr;
-  const size_t smem = (size_t)(3 * (int64_t)G * dk + (int64_t)G * RP * dv) * sizeof(float);
+  const size_t smem = (size_t)(3 * (int64_t)G * dk + gla_pad4(3 * (int64_t)G * dk) + (int64_t)G * RP * dv) *
+                      sizeof(float);
   void (*fn)(GlaParams);
   if (small) {
     fn = dtype == GLA_F16 ? gla_decode_kernel_small<F16>

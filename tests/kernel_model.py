@@ -350,6 +350,30 @@ def staged_shifted(a, j0, seglen, off, as_elems):
 
 
 
+def gla_partial_store_conflicts(cpr, vec, dv):
+    """Bank-conflict count of the GLA partial stores (``store_partials``):
+    a warp's lanes (column chunk cc = lane % cpr, row block lane // cpr) each
+    store VEC floats at float offset (row block * dv + cc * vec) as 16-byte
+    vectors -- for VEC = 8 the half (bit 5 of the offset) first.  Each store
+    instruction is served in phases of 8 lanes; a phase conflicts where two
+    lanes hit the same 16-byte bank group (offset / 4 mod 8).  Returns the
+    number of extra wavefronts over the warp's stores."""
+    extra = 0
+    halves = vec // 4
+    for step in range(halves):
+        for phase in range(4):
+            groups = []
+            for lane in range(8 * phase, 8 * phase + 8):
+                cc, rb = lane % cpr, lane // cpr
+                base = rb * dv + cc * vec
+                h = step if vec == 4 else (step ^ ((base >> 5) & 1))
+                off = base + 4 * h
+                assert off % 4 == 0
+                groups.append((off // 4) % 8)
+            extra += max(groups.count(gr) for gr in set(groups)) - 1
+    return extra
+
+
 def gla_balanced_grid(units, cap):
     """The host's grid for `units` rounds dealt round-robin over at most
     `cap` resident CTAs: the fewest rounds per CTA, then the fewest CTAs --
@@ -393,7 +417,8 @@ def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=None, grid=No
     TPG = threads // G
     RP = TPG // cpr
     assert RP >= 1
-    smem_floats = 3 * G * dk + G * RP * dv
+    P0 = 3 * G * dk + (-(3 * G * dk)) % 4  # partials start on a 16-byte boundary
+    smem_floats = P0 + G * RP * dv
     rounds = -(-bh // G)
     grid = rounds if grid is None else min(grid, rounds)
     touched = np.zeros((bh, dk, dv), dtype=np.int32)
@@ -417,14 +442,14 @@ def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=None, grid=No
                             assert 0 <= vidx < bh * dk * cpr
                             assert 2 * G * dk + gi * dk + i < 3 * G * dk  # qq[gi][i], the last staged array
                             touched[h, i, cc * vec:(cc + 1) * vec] += 1
-                base = 3 * G * dk + (gi * RP + rl) * dv + cc * vec
-                assert base + vec <= smem_floats
+                base = P0 + (gi * RP + rl) * dv + cc * vec
+                assert base + vec <= smem_floats and base % 4 == 0  # 16-byte vector stores
                 part_written.update(range(base, base + vec))
                 assert (h * dv) // vec + cc < bh * dv // vec
             for x in range(nh * dv):
                 g, j = divmod(x, dv)
                 for rb in range(RP):
-                    assert 3 * G * dk + (g * RP + rb) * dv + j in part_written
+                    assert P0 + (g * RP + rb) * dv + j in part_written
                 o_written[h0 + g, j] += 1
     assert (touched == 1).all() and (o_written == 1).all()
     return {"smem_floats": smem_floats, "heads_per_cta": G}
@@ -453,9 +478,8 @@ def gla_pipe_ok(dk, dv, elem_bytes):
 
 def gla_auto_is_pipe(dk, dv, elem_bytes):
     """The automatic choice (aligned pointers assumed): the pipelined layout
-    for heads of more than 1024 16-byte chunks where it applies, else the
-    CTA layout."""
-    return gla_pipe_ok(dk, dv, elem_bytes) and dk * (dv * elem_bytes // 16) > 1024
+    where it applies, else the CTA layout."""
+    return gla_pipe_ok(dk, dv, elem_bytes)
 
 
 def gla_pipe_heads_per_cta(bh, dk, dv, elem_bytes, threads=256):
@@ -563,7 +587,7 @@ def replay_gla_pipe(bh, dk, dv, elem_bytes, threads=256, grid=None):
                         assert cur[qsm][0] == "qkg"[a]
                         assert cur[qsm][1] * 16 // elem_bytes + (x * elem_bytes % 16) // elem_bytes == h * dk + i
                 base = 2 * BUF * 16 + ((gi * RP + rl) * dv + cc * vec) * 4
-                assert base + 4 * vec <= smem
+                assert base + 4 * vec <= smem and base % 16 == 0
             for x in range(nh * dv):
                 g, jj = divmod(x, dv)
                 o_written[h0 + g, jj] += 1

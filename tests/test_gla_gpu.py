@@ -127,7 +127,7 @@ def test_gla_in_place(cuda_dev, dtype, variant):
 def test_gla_layouts_agree(cuda_dev, bh, dk, dv, dtype):
     """The layouts store bit-identical states (same fmaf per element) and o
     within the sum-order tolerance; the automatic choice is the pipelined
-    layout for large heads where it applies, else the CTA layout."""
+    layout where it applies, else the CTA layout."""
     q, k, v, gk, S = _make(bh, dk, dv, dtype, 21, cuda_dev)
     S_c, o_c = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_CTA)
     S_w, o_w = g.gla_decode(q, k, v, gk, S, scale=0.25, variant=g.GLA_VARIANT_WARP)

@@ -270,12 +270,23 @@ def test_gla_pipe_choice():
     assert hp(2048, 128, 128, 2) == 1 and hp(4096, 64, 64, 2) == 2 and hp(16384, 16, 64, 2) == 8
     assert hp(8192, 64, 64, 4) == 2
     auto = kernel_model.gla_auto_is_pipe
-    assert auto(128, 128, 2) and not auto(64, 64, 2) and not auto(16, 64, 2) and not auto(128, 128, 4)
+    assert auto(128, 128, 2) and auto(64, 64, 2) and auto(16, 64, 2) and not auto(128, 128, 4)
+    assert not auto(256, 256, 2) and not auto(5, 64, 2)
     for bh, dk, dv, es in [(2048, 128, 128, 2), (4096, 64, 64, 2), (16384, 16, 64, 2), (2048, 64, 64, 4),
                            (5, 8, 2048, 2), (64, 2048, 8, 2)]:
         if ok(dk, dv, es):
             smem = kernel_model.gla_pipe_smem(hp(bh, dk, dv, es), dk, dv, es)
             assert 3 * (smem + 1024) <= 233472, (bh, dk, dv, smem)
+
+
+@pytest.mark.parametrize("cpr,vec", [(16, 8), (8, 8), (32, 8), (4, 8), (2, 8), (1, 8), (3, 8), (5, 8), (16, 4),
+                                     (32, 4), (8, 4), (2, 4)])
+def test_gla_partial_stores_conflict_free(cpr, vec):
+    """The 16-byte partial stores, in the order ``store_partials`` issues
+    them, hit 8 distinct bank groups in every 8-lane phase (the naive order
+    for 8 floats per lane conflicts 2-way)."""
+    dv = cpr * vec
+    assert kernel_model.gla_partial_store_conflicts(cpr, vec, dv) == 0
 
 
 def test_gla_heads_per_cta_choice():
