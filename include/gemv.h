@@ -400,7 +400,7 @@ enum {
                                into a second shared-memory buffer by asynchronous copies while the
                                current round computes; needs dk * element size a multiple of 16,
                                q, k, gk 16-byte aligned, dk * dv * element size <= 32 KiB and its
-                               two buffers within 75 KiB of shared memory.  S_new bit-identical to
+                               two buffers within 110 KiB of shared memory.  S_new bit-identical to
                                GLA_VARIANT_CTA; o too where both take the same heads per round */
 };
 

@@ -302,9 +302,12 @@ __global__ void __launch_bounds__(kGlaThreads, 3) gla_decode_kernel_small(GlaPar
 // round's state (or, with GLA_PREFETCH_STATE, every thread already copies
 // its part of it): measured 3-8 % faster back to back.
 constexpr int kGlaPipeRoundChunks = 2048;
-// Shared memory of one CTA at most: three CTAs per SM (228 KB, 1 KB reserved
-// per CTA).
-constexpr int64_t kGlaPipeMaxSmem = 75 * 1024;
+// Shared memory of one CTA at most: two CTAs per SM (228 KB, 1 KB reserved
+// per CTA).  More heads per round measured faster than more CTAs per SM:
+// 4096 x 64 x 64 fp16 13.8 us with 4 heads per round and 2 CTAs per SM
+// against 15.0 us with 2 heads and 4 CTAs; one CTA per SM with rounds of
+// up to 4096 chunks was slower on every workload (16.1 us here).
+constexpr int64_t kGlaPipeMaxSmem = 110 * 1024;
 
 int64_t gla_pipe_smem(int G, int64_t dk, int64_t dv, int cpr, int es) {
   const int RP = (kGlaThreads / G) / cpr;

@@ -458,7 +458,7 @@ def replay_gla(bh, dk, dv, elem_bytes, threads=256, rows_in_flight=None, grid=No
 GLA_PIPE_ROUND_CHUNKS = 2048
 
 
-GLA_PIPE_MAX_SMEM = 75 * 1024
+GLA_PIPE_MAX_SMEM = 110 * 1024
 
 
 def gla_pipe_smem(G, dk, dv, elem_bytes, threads=256):
