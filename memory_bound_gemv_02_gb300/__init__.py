@@ -183,8 +183,9 @@ def gemv(B: torch.Tensor, a: torch.Tensor, c: torch.Tensor | None = None, out_fp
          stream=None) -> torch.Tensor:
     """c = B @ a on B's device, asynchronously on ``stream`` (default: the
     current torch stream), launched as a programmatic dependent launch that
-    touches no memory before the preceding kernel has completed.  Returns c
-    (allocated if not given)."""
+    reads and writes no memory before the preceding kernel has completed (it
+    only asks L2 to prefetch its first tile of B).  Returns c (allocated if
+    not given)."""
     n, k, c = _operands(B, a, c, out_fp32)
     with torch.cuda.device(B.device):
         st = lib().gemv(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k,
