@@ -17,10 +17,11 @@
 // k_i v_j) in fp32, store it rounded once, and accumulate q_i * S_new_ij
 // (unrounded) for their columns.  The RP row partials of each column are
 // added in shared memory in row-block order, so the result is deterministic.
-// Four rows are in flight per thread; the first four are requested before
-// the round's staging, so their latency overlaps it.  A pipelined form
-// (gla_decode_pipe_kernel) copies the next round into shared memory while
-// the current one computes.
+// Four rows (large heads) or eight (small heads) are in flight per thread;
+// the first batch is requested before the round's staging, so their
+// latency overlaps it.  A pipelined form (gla_decode_pipe_kernel, the
+// automatic choice where it applies) copies the next round into shared
+// memory while the current one computes.
 // S_new may be S itself (an in-place step): every element is read and then
 // written by the same thread.
 #include <cuda_runtime.h>
@@ -39,7 +40,7 @@ struct GlaParams {
   int64_t bh;
   int32_t dk, dv;
   float scale;
-  int32_t heads_per_cta;  // gla_decode_kernel: heads processed side by side per round (G)
+  int32_t heads_per_cta;  // CTA layouts: heads processed side by side per round (G)
   int32_t early_state;    // GLA_PREFETCH_STATE: S is unwritten by the work in flight
 };
 
@@ -104,9 +105,6 @@ struct GlaIo<F32> {
 };
 
 constexpr int kGlaThreads = 256;
-
-// Floats to add after x floats to reach a multiple of 4 (16 bytes).
-__host__ __device__ constexpr int gla_pad4(int64_t x) { return (int)((4 - (x & 3)) & 3); }
 constexpr int kGlaMaxDk = 4096;
 // Rows of 16-byte chunks in flight per thread in the CTA layout: 8 for heads
 // of at most kGlaSmallHeadChunks chunks (with registers capped for 3 CTAs
@@ -116,6 +114,9 @@ constexpr int kGlaMaxDk = 4096;
 constexpr int kGlaRowsInFlight = 4;
 constexpr int kGlaRowsInFlightSmall = 8;
 constexpr int64_t kGlaSmallHeadChunks = 1024;
+
+// Floats to add after x floats to reach a multiple of 4 (16 bytes).
+__host__ __device__ constexpr int gla_pad4(int64_t x) { return (int)((4 - (x & 3)) & 3); }
 
 // 16-byte store of data written once (no L1 allocation needed).
 __device__ __forceinline__ void stg_stream(uint4 *p, const uint4 &v) {
@@ -309,6 +310,8 @@ constexpr int kGlaPipeRoundChunks = 2048;
 // up to 4096 chunks was slower on every workload (16.1 us here).
 constexpr int64_t kGlaPipeMaxSmem = 110 * 1024;
 
+// Dynamic shared memory of the pipelined layout: two buffers of a round's
+// state, q, k, gk and v (16-byte chunks), then o's row-block partials.
 int64_t gla_pipe_smem(int G, int64_t dk, int64_t dv, int cpr, int es) {
   const int RP = (kGlaThreads / G) / cpr;
   const int64_t buf = (int64_t)G * dk * cpr + 3 * ((int64_t)G * dk * es / 16) + (int64_t)G * cpr;
