@@ -232,6 +232,22 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     rows_of(0, g0, valid);
     tile_issue<U, R>(bal, g0, valid, t0 + lane, t1, bv);
     prefetched = true;
+    if (early) {
+      // B is promised unwritten: also ask L2 for the blocks of the warp's
+      // second step (the next 32*U blocks of its rows' slices, or, for a
+      // slice of one step, the first step of its rows in tile 1), so that
+      // HBM keeps streaming while the CTA waits for the predecessor and
+      // stages a.  Lane r issues row r's.
+      int b0 = t0 + 32 * U;
+      if (b0 >= t1) {
+        rows_of(1, g0, valid);
+        b0 = t0;
+      }
+      const int b1 = (b0 + 32 * U) < t1 ? (b0 + 32 * U) : t1;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (lane == r && valid[r] && b1 > b0) prefetch_l2(bal + g0[r] + b0, (uint32_t)(b1 - b0) * 16u);
+    }
   }
   for (int m = 1; m <= pf; ++m) prefetch_tile(m);
   // a is staged before the wait only when the caller promised that the
