@@ -570,7 +570,13 @@ def run_gla(args, dev):
 def run_case(args, dev):
     """Run one shape a few times and exit (for profiler captures):
     --case N,K,DTYPE[,f32] [--calls C] [--config JSON] [--epilogue ACT]
-    (ACT: run gemv_fused with alpha 0.5, an fp32 bias and that activation)."""
+    (ACT: run gemv_fused with alpha 0.5, an fp32 bias and that activation).
+    With --range R, R more calls follow back to back between
+    cudaProfilerStart and cudaProfilerStop, alternating copies of B that
+    together exceed L2 (as the timed calls do).  With --graph as well, the R
+    calls are captured in a CUDA graph and the range is one replay of it, so
+    that a profiler taking whole graphs as its unit measures consecutive
+    launches together, with their programmatic overlap."""
     import torch
 
     import memory_bound_gemv_02_gb300 as g
@@ -582,14 +588,73 @@ def run_case(args, dev):
     c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
     cfg = json.loads(args.config) if args.config else None
     bias = torch.linspace(-1, 1, n, device=dev) if args.epilogue else None
-    for _ in range(args.calls):
+
+    def call(Bx):
         if args.epilogue:
-            g.gemv_fused(B, a, c=c, out_fp32=out_fp32, alpha=0.5, beta=1.0, bias=bias, activation=args.epilogue,
+            g.gemv_fused(Bx, a, c=c, out_fp32=out_fp32, alpha=0.5, beta=1.0, bias=bias, activation=args.epilogue,
                          config=cfg)
         else:
-            g.gemv_ex(B, a, c=c, out_fp32=out_fp32, config=cfg)
+            g.gemv_ex(Bx, a, c=c, out_fp32=out_fp32, config=cfg)
+
+    for _ in range(args.calls):
+        call(B)
     torch.cuda.synchronize()
-    print(json.dumps({"case": args.case, "calls": args.calls, "epilogue": args.epilogue,
+    graph_us = None
+    if args.range:
+        copies = max(2, min(16, -(-3 * L2_BYTES // max(1, n * k * 2))))
+        Bs = [B] + [B.clone() for _ in range(copies - 1)]
+        for i in range(len(Bs)):  # every copy once before the range
+            call(Bs[i])
+        # raw C-ABI calls (the launch configuration built once), so the
+        # host enqueues far faster than the GPU runs them
+        L = g.lib()
+        fc = g.GemvConfig()
+        for key, val in (cfg or {}).items():
+            setattr(fc, key, val)
+        dt = g.dtype_code(B.dtype, out_fp32)
+        st = torch.cuda.current_stream().cuda_stream
+        if cfg is None:  # gemv()'s own launch
+            fn = L.gemv
+            raw = [(Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, st) for Bx in Bs]
+        else:
+            fn = L.gemv_ex
+            raw = [(Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(fc), st) for Bx in Bs]
+        torch.cuda.synchronize()
+
+        def run_range():
+            for i in range(args.range):
+                if args.epilogue:
+                    call(Bs[i % len(Bs)])
+                elif fn(*raw[i % len(raw)]) != 0:
+                    raise RuntimeError("gemv failed inside the profiler range")
+
+        if args.graph:
+            # the same calls captured once into a CUDA graph (programmatic
+            # launches become programmatic edges) and replayed as one unit
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                st = torch.cuda.current_stream().cuda_stream
+                raw = [r[:-1] + (st,) for r in raw]
+                run_range()
+            gr.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            graph_us = e0.elapsed_time(e1) * 1e3 / args.range
+            torch.cuda.profiler.start()
+            gr.replay()
+            torch.cuda.synchronize()
+            torch.cuda.profiler.stop()
+        else:
+            torch.cuda.profiler.start()
+            run_range()
+            torch.cuda.synchronize()
+            torch.cuda.profiler.stop()
+    print(json.dumps({"case": args.case, "calls": args.calls, "range": args.range, "graph": bool(args.graph),
+                      "graph_us_per_call": graph_us, "epilogue": args.epilogue,
                       "config": g.gemv_last_config()}))
     return 0
 
@@ -791,6 +856,10 @@ def main(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--case", default=None, help="N,K,DTYPE[,f32]: run that shape --calls times, no timing")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--range", type=int, default=0,
+                    help="with --case: R more calls back to back inside a cudaProfilerStart/Stop range")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --range: capture the R calls in a CUDA graph; the range is one replay of it")
     ap.add_argument("--gla", action="store_true", help="time the GLA decode step workloads instead")
     ap.add_argument("--gla-steps", type=int, default=300)
     ap.add_argument("--config", default=None, help="JSON launch configuration forced with --case")
