@@ -570,7 +570,8 @@ def run_gla(args, dev):
 def run_case(args, dev):
     """Run one shape a few times and exit (for profiler captures):
     --case N,K,DTYPE[,f32] [--calls C] [--config JSON] [--epilogue ACT]
-    (ACT: run gemv_fused with alpha 0.5, an fp32 bias and that activation).
+    [--b-offset E] (ACT: run gemv_fused with alpha 0.5, an fp32 bias and
+    that activation; E: B starts E elements past a 512-byte boundary).
     With --range R, R more calls follow back to back between
     cudaProfilerStart and cudaProfilerStop, alternating copies of B that
     together exceed L2 (as the timed calls do).  With --graph as well, the R
@@ -585,6 +586,12 @@ def run_case(args, dev):
     n, k, dtype = int(parts[0]), int(parts[1]), parts[2]
     out_fp32 = len(parts) > 3 and parts[3] == "f32"
     B, a = inputs.make_inputs(n, k, dtype, "normal", 0, dev)
+    if args.b_offset:
+        # the same matrix at an element offset past a 512-byte boundary
+        buf = torch.empty(n * k + args.b_offset, dtype=B.dtype, device=dev)
+        Bo = buf[args.b_offset:].view(n, k)
+        Bo.copy_(B)
+        B = Bo
     c = torch.empty(n, dtype=torch.float32 if out_fp32 else B.dtype, device=dev)
     cfg = json.loads(args.config) if args.config else None
     bias = torch.linspace(-1, 1, n, device=dev) if args.epilogue else None
@@ -602,7 +609,11 @@ def run_case(args, dev):
     graph_us = None
     if args.range:
         copies = max(2, min(16, -(-3 * L2_BYTES // max(1, n * k * 2))))
-        Bs = [B] + [B.clone() for _ in range(copies - 1)]
+        Bs = [B]
+        for _ in range(copies - 1):  # each copy at B's offset
+            buf = torch.empty(n * k + args.b_offset, dtype=B.dtype, device=dev)
+            Bs.append(buf[args.b_offset:].view(n, k))
+            Bs[-1].copy_(B)
         for i in range(len(Bs)):  # every copy once before the range
             call(Bs[i])
         # raw C-ABI calls (the launch configuration built once), so the
@@ -653,7 +664,8 @@ def run_case(args, dev):
             run_range()
             torch.cuda.synchronize()
             torch.cuda.profiler.stop()
-    print(json.dumps({"case": args.case, "calls": args.calls, "range": args.range, "graph": bool(args.graph),
+    print(json.dumps({"case": args.case, "calls": args.calls, "b_offset": args.b_offset, "range": args.range,
+                      "graph": bool(args.graph),
                       "graph_us_per_call": graph_us, "epilogue": args.epilogue,
                       "config": g.gemv_last_config()}))
     return 0
@@ -858,6 +870,8 @@ def main(argv=None):
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--range", type=int, default=0,
                     help="with --case: R more calls back to back inside a cudaProfilerStart/Stop range")
+    ap.add_argument("--b-offset", type=int, default=0,
+                    help="with --case: B starts this many elements past a 512-byte boundary")
     ap.add_argument("--graph", action="store_true",
                     help="with --range: capture the R calls in a CUDA graph; the range is one replay of it")
     ap.add_argument("--gla", action="store_true", help="time the GLA decode step workloads instead")

@@ -151,8 +151,11 @@ bool valid_tiles_RU(int R, int U) {
 
 // Warps per row (S) of the tiles kernel for rows of nt 16-byte blocks: the
 // smallest power-of-two split whose slices are at most 1024 blocks (16 KB
-// per warp and row; longer slices measured 4-10 % slower at k = 16384) and
-// that gives at least 80 % of the resident warps (sm x 32) a slice, without
+// per warp and row; longer slices measured 4-10 % slower at k = 16384) plus
+// the at most 32 blocks the kernel folds into a slice's last step (so the
+// extra edge block of an unaligned row does not double S: 7168 x 16384 at
+// an odd element offset 38.1 us with S = 4, slices of 513 blocks) and that
+// gives at least 80 % of the resident warps (sm x 32) a slice, without
 // cutting slices below 128 blocks.  Measured on GB300 against every (W, S,
 // R) over the workload shapes: this choice is the fastest or within 3 % of
 // it.
@@ -163,7 +166,7 @@ bool valid_tiles_RU(int R, int U) {
 // keeps doubling as long as that fills the rounds better (300 x 100003: 4
 // warps per row 21.0 us, 16 warps per row 18.8 us).
 int tiles_split(int64_t n, int64_t nt, int W, int sm, int64_t Sg, int NCLS, int cps_warps) {
-  int S = (int)pow2_ceil(cdiv(nt, 1024));
+  int S = (int)pow2_ceil(cdiv(nt, 1024 + 32));
   if (S > W) S = W;
   const int64_t fill = (int64_t)sm * 32 * 4 / 5;
   while (2 * S <= W && n * S * Sg < fill && cdiv(nt, 2 * S) >= 128) S *= 2;

@@ -234,15 +234,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     prefetched = true;
     if (early) {
       // B is promised unwritten: also ask L2 for the blocks of the warp's
-      // second step (the next 32*U blocks of its rows' slices, or, for a
-      // slice of one step, the first step of its rows in tile 1), so that
-      // HBM keeps streaming while the CTA waits for the predecessor and
-      // stages a.  Lane r issues row r's.
-      int b0 = t0 + 32 * U;
-      if (b0 >= t1) {
-        rows_of(1, g0, valid);
-        b0 = t0;
-      }
+      // second step (the next 32*U blocks of its rows' slices), so that HBM
+      // keeps streaming while the CTA waits for the predecessor and stages
+      // a.  Lane r issues row r's.  (A slice of one step prefetches
+      // nothing: asking for the first step of the next tile's rows instead
+      // measured 2-4 % slower at k = 1000.)
+      const int b0 = t0 + 32 * U;
       const int b1 = (b0 + 32 * U) < t1 ? (b0 + 32 * U) : t1;
 #pragma unroll
       for (int r = 0; r < R; ++r)
@@ -279,6 +276,26 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     for (int t = t0 + lane; t < t1; t += 32 * U) {
       if (!prefetched) tile_issue<U, R>(bal, g0, valid, t, t1, bv);
       prefetched = false;
+      // A last step of at most one block per lane (the extra edge block of
+      // an unaligned row makes a slice 32*U*m + 1 blocks long) is folded
+      // into this one: its loads go out with this step's, saving a whole
+      // memory round trip.  The blocks are added in the same order as in a
+      // step of their own.
+      const int tx = t + 32 * U;
+      const int rem = t1 - (tx - lane);  // blocks after this step (warp-uniform)
+      if (R <= 2 && rem > 0 && rem <= 32) {
+        uint4 bx[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) bx[r] = (tx < t1 && valid[r]) ? ldg_stream(bal + g0[r] + tx) : zero4();
+        tile_consume<T, U, R, NA>(as4, bv, t, t1, acc);
+        if (tx < t1) {
+          float af[8];
+          widen8<T>(as4[tx], af);
+#pragma unroll
+          for (int r = 0; r < R; ++r) fma8<T, NA>(bx[r], af, acc[r]);
+        }
+        break;
+      }
       tile_consume<T, U, R, NA>(as4, bv, t, t1, acc);
     }
     prefetched = false;

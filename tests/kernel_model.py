@@ -150,19 +150,16 @@ def replay_tiles(n, k, cfg, base_off=0, ldb=None):
         stage_col = stage_x - off  # segment column held by staged element x
         if ngroups > 0:
             # L2 prefetch of the second step, issued with B promised unwritten:
-            # the next 32*U blocks of the first tile's row slices, or tile 1's
-            # first step when a slice has one step only.  Every prefetched
-            # block must be a block of that row's own slice.
+            # the next 32*U blocks of the first tile's row slices.  Every
+            # prefetched block must be a block of that row's own slice.
             for warp in range(W):
                 slot, s = divmod(warp, S)
                 t0 = min(s * L, nt)
                 t1 = min(t0 + L, nt)
-                b0, g = t0 + 32 * U, 0
-                if b0 >= t1:
-                    b0, g = t0, 1
+                b0 = t0 + 32 * U
                 b1 = min(b0 + 32 * U, t1)
                 for r in range(R):
-                    m = g * RT + slot * R + r
+                    m = slot * R + r
                     if m >= nloc or b1 <= b0:
                         continue
                     i = NCLS * (cq + Cq * m) + cls
