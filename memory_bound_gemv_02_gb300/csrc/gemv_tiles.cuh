@@ -232,13 +232,16 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     rows_of(0, g0, valid);
     tile_issue<U, R>(bal, g0, valid, t0 + lane, t1, bv);
     prefetched = true;
-    if (early) {
-      // B is promised unwritten: also ask L2 for the blocks of the warp's
-      // second step (the next 32*U blocks of its rows' slices), so that HBM
-      // keeps streaming while the CTA waits for the predecessor and stages
-      // a.  Lane r issues row r's.  (A slice of one step prefetches
-      // nothing: asking for the first step of the next tile's rows instead
-      // measured 2-4 % slower at k = 1000.)
+    // Also ask L2 for the blocks of the warp's second step (the next 32*U
+    // blocks of its rows' slices), so that HBM keeps streaming while the
+    // CTA stages a.  With B promised unwritten this goes out before the
+    // wait on the predecessor; otherwise (issued after the wait, like the
+    // first step's loads) only when the CTA streams more than one row tile
+    // (4096 x 4096, a single tile per CTA, measured 6 % slower with it).
+    // Lane r issues row r's.  A slice of one step prefetches nothing
+    // (asking for the first step of the next tile's rows instead measured
+    // 2-4 % slower at k = 1000).
+    if (early || ngroups > 1) {
       const int b0 = t0 + 32 * U;
       const int b1 = (b0 + 32 * U) < t1 ? (b0 + 32 * U) : t1;
 #pragma unroll
