@@ -78,9 +78,9 @@ enum {
                                     completion tracked by one mbarrier per buffer.  The
                                     sm_103a form of the multi-stage shared-memory pipeline of
                                     B (TileLang Case Studies, Case B.1 "O3 Pipelined B
-                                    Loads").  Used only when forced: the planner always
-                                    picks the tiles variant, which measured as fast or
-                                    faster on GB300 as gemv() launches them */
+                                    Loads").  The planner picks it for B of 768 MiB or more
+                                    when the tiles plan has one warp per row (rows of at
+                                    most 1024 16-byte blocks); otherwise only when forced */
 };
 
 /* Launch overlap with the preceding work on the stream (gemv_config.overlap). */
