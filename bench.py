@@ -269,9 +269,11 @@ def oracle_rows_rate(B_bits, a_bits, fmt, budget_s: float, rows_cap=None):
 def cpu_baseline(B_bits, a_bits, fmt, n, k, out_bytes, budget_s=12.0):
     rows, secs = oracle_rows_rate(B_bits, a_bits, fmt, budget_s)
     bytes_done = rows * k * 2 + k * 2 + rows * out_bytes
-    return {"value": round(bytes_done / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(bytes_done / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "us_per_call": round(secs / (rows / n) * 1e6, 1),
             "sample": f"{rows} rows of the {n}x{k} matrix ({rows / n:.2f} passes), "
-                      f"{secs:.1f} s single-threaded fp64 C loop"}
+                      f"{secs:.1f} s single-threaded fp64 C loop on 1 of {os.cpu_count()} host cores"}
 
 
 # ---------------------------------------------------------- reference arm --
