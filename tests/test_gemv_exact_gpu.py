@@ -90,6 +90,36 @@ def test_integer_inputs_bit_exact(cuda_dev, dtype, out_fp32, cfg):
         assert exact_bits_match(c, B, a, out_fp32), (n, k, cfg)
 
 
+# Slices whose last step holds at most one block per lane (32 blocks) are
+# folded into the step before; 33 blocks are not.  Row lengths (in 16-byte
+# blocks) of 32*U*m + {1, 2, 32, 33} with U = 8 (steps of 256 blocks) and
+# U = 4 (128), for one and two warps per row; k % 8 != 0 adds the edge block
+# of unaligned rows.
+FOLD_K = [1032, 1288, 2049, 2056, 2304, 2328, 4104, 4112, 4113]
+FOLD_CONFIGS = [{"variant": 3, "warp_split": 1, "rows_per_warp": 1, "unroll": 8},
+                {"variant": 3, "warp_split": 1, "rows_per_warp": 2, "unroll": 4},
+                {"variant": 3, "warp_split": 2, "rows_per_warp": 1, "unroll": 8}]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("cfg", FOLD_CONFIGS)
+def test_folded_last_step_bit_exact(cuda_dev, dtype, cfg):
+    """The fold, and its boundary (a remainder of 33 blocks is a step of its
+    own), in every launch mode (the second step's L2 prefetch differs between
+    them) and at a B offset: integer inputs, so the output is bit-exact."""
+    for k in FOLD_K:
+        B, a = inputs.make_int_inputs(300, k, dtype, seed=k, device=cuda_dev)
+        buf = torch.zeros(300 * k + 8, dtype=B.dtype, device=cuda_dev)
+        Bo = buf[3:3 + 300 * k].view(300, k)
+        Bo.copy_(B)
+        for Bx in (B, Bo):
+            for overlap in (0, 1, 2):
+                c = _run_valid(Bx, a, False, {**cfg, "overlap": overlap})
+                if c is None:
+                    continue
+                assert exact_bits_match(c, Bx, a, False), (k, cfg, overlap, Bx.data_ptr() % 16)
+
+
 TAIL_N = [1, 2, 3, 7, 8, 9, 16, 17, 31, 32, 33, 255, 256, 257]
 TAIL_K = [1, 2, 5, 8, 9, 15, 16, 17, 31, 33, 255, 256, 257, 4099]
 

@@ -438,3 +438,15 @@ def test_long_rows_replay(gemv_lib, n, k, base_off):
     for variant in (None, 4):
         cfg = gemv_lib.gemv_plan(n, k, 0, base_off == 0, SM, config={"variant": variant} if variant else None)
         kernel_model.replay(n, k, cfg, base_off=base_off)
+
+
+@pytest.mark.parametrize("cfg", [{"variant": 3, "warp_split": 1, "rows_per_warp": 1, "unroll": 8},
+                                 {"variant": 3, "warp_split": 1, "rows_per_warp": 2, "unroll": 4},
+                                 {"variant": 3, "warp_split": 2, "rows_per_warp": 1, "unroll": 8}])
+@pytest.mark.parametrize("base_off", [0, 3])
+def test_folded_step_plans_replay(gemv_lib, cfg, base_off):
+    """The forced plans of the folded-last-step GPU test, replayed in full
+    before they run (row lengths of 32*U*m + {1, 2, 32, 33} blocks)."""
+    for k in [1032, 1288, 2049, 2056, 2304, 2328, 4104, 4112, 4113]:
+        p = gemv_lib.gemv_plan(300, k, 0, base_off == 0, SM, config=cfg)
+        kernel_model.replay(300, k, p, base_off=base_off)
