@@ -315,8 +315,10 @@ def run_reference(args, world, rank):
         "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "sample_rows_per_step": m},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{m} rows of {n} per step, single-threaded fp64 C loop"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{m} rows of {n} per step, single-threaded fp64 C loop on 1 of "
+                                   f"{os.cpu_count()} host cores"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
