@@ -269,6 +269,18 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
           R = 2;
           U = 4;
         }
+      } else if (!f->warp_split && S >= 2 && U == 8 && 2 * S <= W && cdiv(nt_est, 2 * S) >= 128) {
+        // Rows split over several warps: two rows per warp with twice the
+        // split instead (same rows per tile, same bytes in flight, half as
+        // many shared-memory reads of a per byte of B; slices still of 128
+        // blocks or more).  Measured on GB300
+        // as gemv() launches them, two repeats: faster on all 11 sweep
+        // shapes where it applies (7168 x 16384 34.06 -> 33.27 us, 4096 x
+        // 14336 19.49 -> 18.69, 4099 x 16384 21.85 -> 20.67, 256 x 262144
+        // 24.61 -> 23.38, 65536 x 16384 294.9 -> 294.0).
+        S *= 2;
+        R = 2;
+        U = 4;
       }
     }
     // row tiles and grid
@@ -313,7 +325,13 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
         if (!bulk && !f->warp_split && !f->rows_per_warp && !f->unroll) {
           const int64_t nt2 = cdiv(kseg, 8) + (aligned ? 0 : 1);
           S = tiles_split(n, nt2, W, sm, Sg, NCLS, cps_warps);
+          R = 1;
           U = cdiv(nt2, S) <= 128 ? 4 : 8;
+          if (S >= 2 && U == 8 && 2 * S <= W && cdiv(nt2, 2 * S) >= 128) {  // as above: two rows per warp
+            S *= 2;
+            R = 2;
+            U = 4;
+          }
           RT = (int64_t)(W / S) * R;
           groups = cdiv(rows_per_class, RT);
         }

@@ -43,8 +43,13 @@ def test_plan_shapes_of_interest(gemv_lib):
     """The plans measured fastest (or within 3 %) on GB300 for the workload
     shapes, back to back with programmatic dependent launch."""
     big = gemv_lib.gemv_plan(7168, 16384, 0, True, SM)
-    assert big["grid_split"] == 1 and big["warp_split"] == 2 and big["variant"] == 3
-    assert big["warps_per_cta"] == 16 and big["rows_per_warp"] == 1 and big["unroll"] == 8
+    assert big["grid_split"] == 1 and big["warp_split"] == 4 and big["variant"] == 3
+    assert big["warps_per_cta"] == 16 and big["rows_per_warp"] == 2 and big["unroll"] == 4
+    # rows split over warps take two rows per warp and twice the split
+    p = gemv_lib.gemv_plan(4096, 14336, 1, True, SM)
+    assert (p["warp_split"], p["rows_per_warp"], p["unroll"]) == (4, 2, 4)
+    p = gemv_lib.gemv_plan(256, 262144, 0, True, SM)
+    assert (p["grid_split"], p["warp_split"], p["rows_per_warp"], p["unroll"]) == (8, 8, 2, 4)
     p = gemv_lib.gemv_plan(18432, 7168, 1, True, SM)
     assert (p["warp_split"], p["rows_per_warp"], p["unroll"]) == (1, 2, 4)
     p = gemv_lib.gemv_plan(14336, 4096, 1, True, SM)
@@ -70,6 +75,7 @@ def test_plan_shapes_of_interest(gemv_lib):
     {"ctas": 16}, {"warps_per_cta": 16, "warp_split": 16}, {"rows_per_warp": 2, "unroll": 4},
 ])
 def test_forced_configs_are_honoured(gemv_lib, cfg):
+    """(1000 x 4096: see also the shapes of the GPU forced-config test below.)"""
     out = gemv_lib.gemv_plan(1000, 4096, 0, True, SM, config=cfg)
     for key, v in cfg.items():
         if key == "ctas":
@@ -450,3 +456,31 @@ def test_folded_step_plans_replay(gemv_lib, cfg, base_off):
     for k in [1032, 1288, 2049, 2056, 2304, 2328, 4104, 4112, 4113]:
         p = gemv_lib.gemv_plan(300, k, 0, base_off == 0, SM, config=cfg)
         kernel_model.replay(300, k, p, base_off=base_off)
+
+
+# The forced configurations of the GPU parity test, on its shape and on long
+# rows, where the planner's own choices (two rows per warp with twice the
+# split) would otherwise apply: every forced field but ctas and grid_split
+# is kept as given.
+GPU_FORCED = [
+    {"variant": 2}, {"rows_per_warp": 2}, {"rows_per_warp": 4}, {"warps_per_cta": 4},
+    {"warps_per_cta": 8, "warp_split": 8}, {"warps_per_cta": 16, "warp_split": 4}, {"grid_split": 2},
+    {"grid_split": 5, "warp_split": 2}, {"ctas": 37, "rows_per_warp": 2}, {"variant": 3},
+    {"variant": 3, "warp_split": 8}, {"variant": 3, "warp_split": 2, "warps_per_cta": 4},
+    {"variant": 3, "warp_split": 2}, {"variant": 3, "warp_split": 1},
+    {"variant": 3, "rows_per_warp": 2, "unroll": 4}, {"variant": 3, "grid_split": 4},
+    {"variant": 3, "l2_prefetch": 1}, {"variant": 3, "l2_prefetch": 3, "warp_split": 2},
+]
+
+
+@pytest.mark.parametrize("cfg", GPU_FORCED)
+@pytest.mark.parametrize("n,k", [(1537, 4096), (7168, 16384), (4096, 14336), (256, 262144)])
+def test_forced_fields_kept(gemv_lib, cfg, n, k):
+    try:
+        out = gemv_lib.gemv_plan(n, k, 0, True, SM, config=cfg)
+    except gemv_lib.GemvError as e:
+        assert e.status == gemv_lib.GEMV_ERR_CONFIG
+        return
+    for key, v in cfg.items():
+        if key not in ("ctas", "grid_split"):
+            assert out[key] == v, (key, out)
