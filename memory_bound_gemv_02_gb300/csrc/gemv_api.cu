@@ -268,6 +268,12 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
         if (round_fill(2LL * W) >= 0.99 * round_fill(W)) {
           R = 2;
           U = 4;
+          // Rows of 1024 blocks or more (k >= 8192; S = 1 allows up to
+          // 1056): two warps per pair of rows, slices of whole 128-block
+          // steps (28672 x 8192 bf16 65.05 -> 63.85 us as gemv() launches
+          // it; at 896 blocks the halves are 3.5 steps and it was slower:
+          // 18432 x 7168 36.6 -> 36.9 us).
+          if (!f->warp_split && nt_est >= 1024 && 2 <= W) S = 2;
         }
       } else if (!f->warp_split && S >= 2 && U == 8 && 2 * S <= W && cdiv(nt_est, 2 * S) >= 128) {
         // Rows split over several warps: two rows per warp with twice the
@@ -397,13 +403,14 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
   if (variant == GEMV_VARIANT_TILES && f == &fz) {
     // Nothing forced: the tiles plan, or the bulk variant where it measured
     // faster on GB300 than the tiles plan: B of 768 MiB or more whose rows
-    // the tiles plan streams with one warp each (rows of at most 1024
-    // blocks; 57344 x 7168: 116.5 -> 114.5 us, 65536 x 7169: 135.3 -> 134.5
-    // us back to back).  Below that, and for longer rows, register
-    // streaming is as fast or faster.
+    // the tiles plan streams with at most one warp each, i.e. a warp split
+    // no larger than its rows per warp (rows of at most ~1024 blocks;
+    // 57344 x 7168: 116.5 -> 114.5 us, 65536 x 7169: 135.3 -> 134.5 us back
+    // to back).  Below that, and for longer rows, register streaming is as
+    // fast or faster.
     int st = plan_tiles(n, k, aligned, sm, f, out);
     const int64_t b_bytes = n * k * 2;
-    if (st == GEMV_OK && out->warp_split == 1 && b_bytes >= kBulkAutoBytes) {
+    if (st == GEMV_OK && out->warp_split <= out->rows_per_warp && b_bytes >= kBulkAutoBytes) {
       gemv_config b{};
       if (plan_tiles(n, k, aligned, sm, f, &b, true) == GEMV_OK) *out = b;
     }
