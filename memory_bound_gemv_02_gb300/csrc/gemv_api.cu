@@ -183,6 +183,22 @@ int tiles_split(int64_t n, int64_t nt, int W, int sm, int64_t Sg, int NCLS, int 
   return S;
 }
 
+// Rows split over several warps with 8 loads per lane: two rows per warp
+// with twice the split instead (same rows per tile, same bytes in flight,
+// half as many shared-memory reads of a per byte of B; slices still of 128
+// blocks or more).  Measured on GB300 as gemv() launches them, two
+// repeats: faster on all 11 sweep shapes where it applies (7168 x 16384
+// 34.06 -> 33.27 us, 4096 x 14336 19.49 -> 18.69, 4099 x 16384 21.85 ->
+// 20.67, 256 x 262144 24.61 -> 23.38, 65536 x 16384 294.9 -> 294.0).
+// Returns true (and updates S, R, U) when it applies.
+bool two_rows_per_warp(int64_t nt, int W, int &S, int &R, int &U) {
+  if (S < 2 || U != 8 || 2 * S > W || cdiv(nt, 2 * S) < 128) return false;
+  S *= 2;
+  R = 2;
+  U = 4;
+  return true;
+}
+
 // Planner of the tiles and bulk variants (pure host arithmetic).
 //  * k-segments: as few as the shared-memory budget allows, more when the
 //    rows alone cannot give every SM work (split-K).
@@ -275,18 +291,8 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
           // 18432 x 7168 36.6 -> 36.9 us).
           if (!f->warp_split && nt_est >= 1024 && 2 <= W) S = 2;
         }
-      } else if (!f->warp_split && S >= 2 && U == 8 && 2 * S <= W && cdiv(nt_est, 2 * S) >= 128) {
-        // Rows split over several warps: two rows per warp with twice the
-        // split instead (same rows per tile, same bytes in flight, half as
-        // many shared-memory reads of a per byte of B; slices still of 128
-        // blocks or more).  Measured on GB300
-        // as gemv() launches them, two repeats: faster on all 11 sweep
-        // shapes where it applies (7168 x 16384 34.06 -> 33.27 us, 4096 x
-        // 14336 19.49 -> 18.69, 4099 x 16384 21.85 -> 20.67, 256 x 262144
-        // 24.61 -> 23.38, 65536 x 16384 294.9 -> 294.0).
-        S *= 2;
-        R = 2;
-        U = 4;
+      } else if (!f->warp_split) {
+        two_rows_per_warp(nt_est, W, S, R, U);
       }
     }
     // row tiles and grid
@@ -333,11 +339,7 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
           S = tiles_split(n, nt2, W, sm, Sg, NCLS, cps_warps);
           R = 1;
           U = cdiv(nt2, S) <= 128 ? 4 : 8;
-          if (S >= 2 && U == 8 && 2 * S <= W && cdiv(nt2, 2 * S) >= 128) {  // as above: two rows per warp
-            S *= 2;
-            R = 2;
-            U = 4;
-          }
+          two_rows_per_warp(nt2, W, S, R, U);
           RT = (int64_t)(W / S) * R;
           groups = cdiv(rows_per_class, RT);
         }
