@@ -91,8 +91,9 @@ enum {
                                  while the preceding kernel drains; it waits for that
                                  kernel's completion (and its memory) before reading or
                                  writing any global memory.  Before the wait it only asks L2
-                                 to prefetch its first tile of B: a hint, which reads nothing
-                                 into the kernel and needs no promise */
+                                 to prefetch its first tile of B (and, right after it, the
+                                 second step of its rows): hints, which read nothing into
+                                 the kernel and need no promise */
   /* "Work still running on the stream", for the two promises below: every
      kernel launched on the stream after its last ordinary operation (a kernel
      launched without the programmatic-serialization attribute, a copy, a memset
@@ -100,8 +101,9 @@ enum {
      they wait for their own predecessor, so a chain of them may all run at
      once; an ordinary operation completes only after everything before it. */
   GEMV_OVERLAP_PDL_PREFETCH_B = 2, /* as GEMV_OVERLAP_PDL, and each CTA streams its first tile
-                                 of B into registers (bulk variant: its first ring buffers
-                                 into shared memory) before waiting.  The caller guarantees
+                                 of B into registers and asks L2 for the next step (bulk
+                                 variant: its first ring buffers into shared memory) before
+                                 waiting.  The caller guarantees
                                  that no work still running on the stream writes B (true
                                  for weights); a and c are still accessed only after the
                                  wait */
