@@ -30,6 +30,9 @@ CONFIGS = [None, {"variant": 2}, {"rows_per_warp": 4}, {"warps_per_cta": 4, "war
            {"variant": 3, "rows_per_warp": 2, "unroll": 4, "warps_per_cta": 8},
            {"variant": 3, "grid_split": 3, "warp_split": 2}, {"variant": 3, "ctas": 8},
            {"variant": 3, "l2_prefetch": 2}, {"variant": 3, "l2_prefetch": 1, "warp_split": 4, "overlap": 2},
+           {"variant": 3, "warp_split": 4, "rows_per_warp": 2, "unroll": 4},
+           {"variant": 3, "warp_split": 8, "rows_per_warp": 2, "unroll": 4},
+           {"variant": 3, "warp_split": 2, "rows_per_warp": 2, "unroll": 4, "overlap": 2},
            {"variant": 4}, {"variant": 4, "stages": 2, "unroll": 4, "warp_split": 2},
            {"variant": 4, "grid_split": 3, "warps_per_cta": 8, "warp_split": 4, "overlap": 2}]
 
@@ -118,6 +121,19 @@ def test_folded_last_step_bit_exact(cuda_dev, dtype, cfg):
                 if c is None:
                     continue
                 assert exact_bits_match(c, Bx, a, False), (k, cfg, overlap, Bx.data_ptr() % 16)
+
+
+def test_benchmark_plan_bit_exact_full_size(cuda_dev):
+    """The benchmark workload's shape in the plan gemv() picks for it (two
+    rows per warp, four warps per pair of rows), with integer inputs: every
+    row bit-exact, in both overlap modes the benchmark reports."""
+    n, k = 7168, 16384
+    B, a = inputs.make_int_inputs(n, k, "f16", seed=5, device=cuda_dev)
+    plan = g.gemv_plan(n, k, g.GEMV_F16, True, torch.cuda.get_device_properties(cuda_dev).multi_processor_count)
+    assert (plan["warp_split"], plan["rows_per_warp"], plan["unroll"]) == (4, 2, 4)
+    for cfg in (None, {"overlap": 2}):
+        c = _run(B, a, False, cfg)
+        assert exact_bits_match(c, B, a, False), cfg
 
 
 TAIL_N = [1, 2, 3, 7, 8, 9, 16, 17, 31, 32, 33, 255, 256, 257]
