@@ -484,3 +484,17 @@ def test_forced_fields_kept(gemv_lib, cfg, n, k):
     for key, v in cfg.items():
         if key not in ("ctas", "grid_split"):
             assert out[key] == v, (key, out)
+
+
+@pytest.mark.parametrize("variant", [None, 3, 4])
+def test_ragged_tail_plans_replay(gemv_lib, variant):
+    """The plans of the GPU ragged-tail test (every n and k in 1..17,
+    31..33, 255..257, 4099, 7169), replayed in full where small."""
+    sizes = list(range(1, 18)) + [31, 32, 33, 255, 256, 257, 4099, 7169]
+    cfg = {"variant": variant} if variant else None
+    for n, k in itertools.product(sizes, sizes):
+        if n > 257 and k > 257:
+            continue
+        p = gemv_lib.gemv_plan(n, k, 0, True, SM, config=cfg)
+        if n * k <= 300000:
+            kernel_model.replay(n, k, p)
