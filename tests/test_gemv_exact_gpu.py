@@ -458,7 +458,8 @@ def test_maximum_k_ones_closed_form(cuda_dev):
     assert (inputs.out_bits(cb) == oracle.round_out(np.array([float(k)]), "bf16")).all()
 
 
-@pytest.mark.parametrize("n,k,dtype", [(3000, 4104, "bf16"), (1_400_000, 16, "f16"), (513, 7169, "f16")])
+@pytest.mark.parametrize("n,k,dtype", [(3000, 4104, "bf16"), (1_400_000, 16, "f16"), (513, 7169, "f16"),
+                                       (2048, 16384, "bf16")])
 def test_shared_input_deferred_stores(cuda_dev, n, k, dtype):
     """GEMV_OVERLAP_PDL_PREFETCH_BA: the tiles kernel keeps its row results
     in shared memory and stores them after one wait (up to 4096 rows per
