@@ -50,6 +50,10 @@ L2_BYTES = 129 * 1000 * 1000
 # Best figure the pages give for this exact workload (fp16, 7168x16384):
 # TileLang Case Studies, Case B.2 table, O1+O2 on an H200: 3.67 TB/s.
 PAGES_BEST_GBS = 3670.0
+# Queue prefill before a timed batch: a sleep kernel of this many SM clock
+# cycles (~1.5 ms at 2 GHz) ahead of the first event, long enough for the
+# host to enqueue hundreds of calls before the GPU reaches the first.
+PREFILL_CYCLES = 3_000_000
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -196,7 +200,7 @@ class ClockSampler:
                 self.proc.kill()
             self.th.join(timeout=2)
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, label="timed region"):
         if not self.lines:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "nvidia-smi unavailable"}
@@ -204,7 +208,7 @@ class ClockSampler:
         rows = [(ln, t) for ln, t in zip(self.lines[1:], self.stamps[1:]) if ln != header]
         inside = [ln for ln, t in rows if t0 <= t <= t1]
         out = parse_clock_rows(header, inside if inside else [ln for ln, _ in rows])
-        out["window"] = "timed region" if inside else "whole run (no sample fell inside the timed region)"
+        out["window"] = label if inside else f"whole run (no sample fell inside the {label})"
         return out
 
 
@@ -340,7 +344,7 @@ def time_calls(L, calls, stream, steps, warmup):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s = torch.cuda.current_stream()
-    torch.cuda._sleep(3_000_000)  # keep the GPU busy while the launches queue up
+    torch.cuda._sleep(PREFILL_CYCLES)  # keep the GPU busy while the launches queue up
     e0.record(s)
     for i in range(steps):
         fn, args = calls[i % len(calls)]
@@ -353,9 +357,11 @@ def time_calls(L, calls, stream, steps, warmup):
     return e0.elapsed_time(e1) / 1e3, per
 
 
-def time_batch(calls, steps, warmup):
+def time_batch(calls, steps, warmup, prefill=True):
     """Run `calls` round-robin back to back with CUDA events only at both
-    ends of the batch; return the elapsed seconds."""
+    ends of the batch; return the elapsed seconds.  ``prefill``: a sleep
+    kernel ahead of the first event keeps the GPU busy while the launches
+    queue up."""
     import torch
     for i in range(warmup):
         fn, args = calls[i % len(calls)]
@@ -364,7 +370,8 @@ def time_batch(calls, steps, warmup):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s = torch.cuda.current_stream()
-    torch.cuda._sleep(3_000_000)  # keep the GPU busy while the launches queue up
+    if prefill:
+        torch.cuda._sleep(PREFILL_CYCLES)
     e0.record(s)
     for i in range(steps):
         fn, args = calls[i % len(calls)]
@@ -394,16 +401,19 @@ def host_overhead_us(L, n, k, dt, dev, stream):
     return statistics.median(per) * 1e6
 
 
-def native_host_overhead():
-    """Host microseconds per cached gemv() call and per empty-kernel launch,
-    measured by the library's native tool (C++, steady_clock, 10^4 calls);
-    None if the tool is not built."""
+def native_measurements(b_bytes: int):
+    """The library's native measurement tool (C++): host microseconds per
+    cached gemv() call and per empty-kernel launch (steady_clock, 10^4
+    calls), and the read-only streaming bandwidth back to back over two 1
+    GiB buffers and over two buffers of ``b_bytes`` (plain launches, and
+    programmatic launches that overlap completely); None if the tool is not
+    built."""
     from memory_bound_gemv_02_gb300 import _build
     if not os.path.exists(_build.HOST_TOOL):
         return None
-    r = subprocess.run([_build.HOST_TOOL], capture_output=True, text=True, timeout=120)
+    r = subprocess.run([_build.HOST_TOOL, str(b_bytes)], capture_output=True, text=True, timeout=300)
     if r.returncode != 0:
-        raise RuntimeError(f"host-overhead tool failed: {r.stdout} {r.stderr}")
+        raise RuntimeError(f"native measurement tool failed: {r.stdout} {r.stderr}")
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
@@ -737,19 +747,23 @@ def run_ours(args, world, rank, local):
     # its first B tile).
     calls = [(L.gemv, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, s)) for Bx in (B, B2)]
 
-    # timed region
-    for i in range(args.warmup):
-        fn, cargs = calls[i % 2]
-        if fn(*cargs) != 0:
-            raise RuntimeError("gemv failed in warm-up")
-    torch.cuda.synchronize()
+    # timed region: the W warm-up calls run right before it (after the clock
+    # sampler has started), then barrier + synchronize, then a queue prefill
+    # (a sleep kernel ahead of the first event, outside the region) so that
+    # the host has enqueued the calls before the GPU reaches them and the
+    # events time the GPU's K calls, not the host's first launch latency.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(dev)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
     with ClockSampler(gpu_id) as clk:
         time.sleep(0.3)  # let the sampler start
+        for i in range(args.warmup):
+            fn, cargs = calls[i % 2]
+            if fn(*cargs) != 0:
+                raise RuntimeError("gemv failed in warm-up")
         barrier(world)
         torch.cuda.synchronize()
+        torch.cuda._sleep(PREFILL_CYCLES)
         t_host0 = time.time()
         ev0.record(stream)
         for i in range(args.steps):
@@ -759,8 +773,16 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         t_host1 = time.time()
         barrier(world)
+        # context, in the same sampler window: the same calls 2000 times,
+        # and K calls without the prefill (the GPU idle when the first
+        # event is recorded)
+        us_2000 = time_batch(calls, 2000, 10) / 2000 * 1e6
+        t_host2 = time.time()
+        us_unprefilled = time_batch(calls, args.steps, 10, prefill=False) / args.steps * 1e6
         time.sleep(0.25)
-    clocks = clk.summary(t_host0, t_host1)
+    # clock samples from the timed region through the 2000-call batch (the
+    # region alone at K = 20 is shorter than one 200 ms sample period)
+    clocks = clk.summary(t_host0, t_host2, "timed region and the 2000-call batch after it")
     elapsed = ev0.elapsed_time(ev1) / 1e3
     elapsed_max = max_over_ranks(elapsed, world)
     value = world * nbytes * args.steps / elapsed_max / 1e9
@@ -775,7 +797,7 @@ def run_ours(args, world, rank, local):
     none_cfg = g.GemvConfig()  # overlap 0
     plain = [(L.gemv_ex, (Bx.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, dt, ctypes.byref(none_cfg), s))
              for Bx in (B, B2)]
-    nplain = min(args.steps, 2000)
+    nplain = 2000
     us_plain = time_batch(plain, nplain, 10) / nplain * 1e6
     pb_cfg = g.GemvConfig()
     pb_cfg.overlap = g.GEMV_OVERLAP_PDL_PREFETCH_B
@@ -814,14 +836,9 @@ def run_ours(args, world, rank, local):
     e2e_value = world * nbytes * e2e_steps / e2e_elapsed / 1e9
     del B_dev, Bh
 
-    # read-only probe (same load path) for context
-    sink = torch.zeros(16384, dtype=torch.int32, device=dev)
-    probe_calls = [(L.gemv_probe_read, (Bx.data_ptr(), n * k * 2, sink.data_ptr(), s)) for Bx in (B, B2)]
-    _, pper = time_calls(L, probe_calls, s, 100, 10)
-    probe_gbs = n * k * 2 / (statistics.median(pper) / 1e3) / 1e9
-
     host_us = host_overhead_us(L, 256, 512, 0, dev, s)
-    native = native_host_overhead()
+    native = native_measurements(n * k * 2)
+    read_ceiling = None if native is None else native["read_gbs_1gib_overlapped"]
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -847,7 +864,17 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(frac_of_peak(achieved, peak), 4), "peak_kind": f"of {peak_kind}",
                      "traffic": profiled_traffic("7168x16384_f16", cfg)},
-        "probe_read_gbs": round(probe_gbs, 1),
+        "us_per_call_2000_calls": round(us_2000, 3),
+        "us_per_call_unprefilled": round(us_unprefilled, 3),
+        "probe_read_gbs": None if read_ceiling is None else round(read_ceiling, 1),
+        "frac_of_read_ceiling": None if read_ceiling is None else round(achieved / read_ceiling, 4),
+        "read_ceiling": None if native is None else {
+            "how": "read-only 16-byte streaming loads, back to back over two buffers, CUDA events after a "
+                   "queue prefill; 'overlapped' = programmatic launches that never wait",
+            "gbs_1gib_overlapped": native["read_gbs_1gib_overlapped"],
+            "gbs_1gib_plain": native["read_gbs_1gib_plain"],
+            "gbs_b_bytes_overlapped": native["read_gbs_small_overlapped"],
+            "gbs_b_bytes_plain": native["read_gbs_small_plain"]},
         "host_us_per_call": round(host_us, 3),
         "host_us_per_call_native": None if native is None else native["gemv_us"],
         "empty_launch_us_native": None if native is None else native["empty_launch_us"],

@@ -20,11 +20,11 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build", "gemv")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgemv.so")
-HOST_TOOL_SRC = "host_overhead_main.cu"
-HOST_TOOL = os.path.join(LIBDIR, "gemv_host_overhead")  # native host-overhead measurement
+HOST_TOOL_SRC = "bench_tool_main.cu"
+HOST_TOOL = os.path.join(LIBDIR, "gemv_bench_tool")  # native host-overhead and read-ceiling measurements
 
 SOURCES = ["gemv_api.cu", "gemv_kernels_f16.cu", "gemv_kernels_bf16.cu", "gemv_bulk_f16.cu", "gemv_bulk_bf16.cu",
-           "gemv_probe.cu", "gla_decode.cu"]
+           "gla_decode.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("gemv_internal.h", "gemv_kernels.cuh", "gemv_tiles.cuh",
                                            "gemv_bulk.cuh")] + \
     [os.path.join(INCLUDE, "gemv.h")]
@@ -78,13 +78,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
-        # the native host-overhead tool, linked against the library just built
+        # the native measurement tool, linked against the library just built
         tmp = HOST_TOOL + f".tmp{os.getpid()}"
         cmd = [exe, *NVCC_FLAGS, *extra_flags, os.path.join(CSRC, HOST_TOOL_SRC), "-o", tmp,
                "-L" + LIBDIR, "-lgemv", "-Xlinker", "-rpath,$ORIGIN"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"host-overhead tool build failed:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"measurement tool build failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, HOST_TOOL)
         return LIB
 

@@ -288,16 +288,6 @@ def test_gemv_host_end_to_end(cuda_dev):
     check_against_oracle(ch.to(cuda_dev), Bd, ad, False, label="gemv_host")
 
 
-def test_probe_checksum(cuda_dev):
-    buf = torch.randint(-2 ** 31, 2 ** 31 - 1, (1 << 22,), dtype=torch.int32, device=cuda_dev)
-    sink = torch.zeros(16384, dtype=torch.int32, device=cuda_dev)
-    g.gemv_probe_read(buf, sink)
-    torch.cuda.synchronize()
-    x = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))
-    y = np.bitwise_xor.reduce(buf.cpu().numpy().view(np.uint32))
-    assert x == y
-
-
 def test_host_overhead_per_call(cuda_dev):
     """A cached-key call costs microseconds of host time (the pages' Case B.4
     saw 11 ms per call from rebuilding a closure).  Measured on the raw
@@ -410,19 +400,25 @@ def test_overlap_prefetch_ba_shared_input(cuda_dev, variant):
     check_against_oracle(c, Bs[-1], a, False, label="last writer of c")
 
 
-def test_native_host_overhead_tool(cuda_dev):
-    """The native (C++) measurement of the host cost of a cached gemv() call:
-    under 10 us, and within a few microseconds of an empty kernel launch."""
+def test_native_measurement_tool(cuda_dev):
+    """The native (C++) measurements beside the benchmark: the host cost of a
+    cached gemv() call is under 10 us and within a few microseconds of an
+    empty kernel launch, and the read-only stream reaches a plausible
+    fraction of the HBM bandwidth (above 3 TB/s, below the 8 TB/s nominal
+    peak plus a margin for the timer)."""
     import json
     import subprocess
 
     from memory_bound_gemv_02_gb300 import _build
-    assert os.path.exists(_build.HOST_TOOL), "the build makes the native host-overhead tool"
-    r = subprocess.run([_build.HOST_TOOL], capture_output=True, text=True, timeout=120)
+    assert os.path.exists(_build.HOST_TOOL), "the build makes the native measurement tool"
+    r = subprocess.run([_build.HOST_TOOL], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     d = json.loads(r.stdout.strip().splitlines()[-1])
     assert 0 < d["gemv_us"] < 10.0
     assert 0 < d["empty_launch_us"] <= d["gemv_us"] + 1.0
+    for key in ("read_gbs_1gib_plain", "read_gbs_1gib_overlapped", "read_gbs_small_plain",
+                "read_gbs_small_overlapped"):
+        assert 3000.0 < d[key] < 8500.0, (key, d[key])
 
 
 @pytest.mark.parametrize("n,k,dtype,cfg", [(2, 3_000_000, "f16", None), (3, 5_000_001, "bf16", None),
