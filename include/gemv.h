@@ -12,10 +12,21 @@
  * the contract (it is fixed for a given shape, dtype and launch
  * configuration, so repeated calls are bitwise reproducible).
  *
+ * Citations name a page and its section: "Case Studies" is the TileOps wiki
+ * page "TileLang Case Studies"; "the DPLR pull request" is "[DPLR] A Tilelang
+ * implementation of DPLR - #1069" (flash-linear-attention); "the
+ * optimization guide" is "Optimizing TileLang Programs".
+ *
  * Conventions shared by every entry point:
  *  - Device pointers are plain CUDA device addresses on the CURRENT device
- *    (cudaGetDevice at the time of the call).  The caller owns B, a and c; the
- *    library never frees or retains them past the call.
+ *    (cudaGetDevice at the time of the call).  The start of every buffer is
+ *    classified with cudaPointerGetAttributes: device memory of another
+ *    device and host memory (pinned, registered or pageable, even where the
+ *    GPU could reach it) return GEMV_ERR_DEVICE before anything is
+ *    launched; managed memory is accepted.  The caller owns every buffer,
+ *    outputs included (preallocated, as the DPLR pull request passes its
+ *    forward outputs to cut host time per call); the library never frees or
+ *    retains them past the call.
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream); the
  *    caller synchronizes before reading c.
  *  - Nothing throws across this boundary and nothing calls exit/abort: every
@@ -24,6 +35,15 @@
  *  - Thread-safe: the launch-configuration cache and workspace table are
  *    guarded internally.  Per-thread state: gemv_last_config, the last CUDA
  *    error code.
+ *  - GEMV_LOG=1 in the environment (read once) prints one line on stderr
+ *    for each launch configuration the planner builds (a key newly cached
+ *    by gemv(), gemv_ex() or gemv_fused() without a forced configuration,
+ *    or by gemv_prepare(); every gemv_plan() call):
+ *      gemv: new config dev=D n=N k=K dtype=T aligned=A -> variant=V
+ *            ctas=C warps_per_cta=W warp_split=S rows_per_warp=R unroll=U
+ *            grid_split=G k_segment=L stages=NS smem_bytes=M
+ *    on one line ("plan" and dev=-1 for gemv_plan()).  Nothing else is
+ *    printed, with or without it.
  */
 #ifndef GEMV_GB300_H_
 #define GEMV_GB300_H_
@@ -50,12 +70,13 @@ enum {
   GEMV_ERR_ARG = -1,     /* null pointer with n > 0 and k > 0, n < 0, k < 0, k > INT32_MAX */
   GEMV_ERR_DTYPE = -2,   /* unknown dtype code */
   GEMV_ERR_ALIAS = -3,   /* c overlaps B or a */
-  GEMV_ERR_DEVICE = -4,  /* no CUDA device, or the current device is not sm_103 */
+  GEMV_ERR_DEVICE = -4,  /* no CUDA device, the current device is not sm_103, or a buffer
+                            is not in the current device's memory (or managed memory) */
   GEMV_ERR_CUDA = -5,    /* a CUDA call or launch failed; see gemv_last_cuda_error() */
   GEMV_ERR_CONFIG = -6,  /* a forced configuration is invalid for this shape */
   GEMV_ERR_ALIGN = -7,   /* B or a not 2-byte aligned, or c not aligned to its element */
   GEMV_ERR_NOMEM = -8,   /* the split-K workspace could not be allocated */
-  GEMV_ERR_SCRATCH = -9  /* gemv_splitk_noalloc: grid_split * n exceeds GEMV_STATIC_SCRATCH_FLOATS */
+  GEMV_ERR_SCRATCH = -9  /* gemv_splitk_noalloc: segments * n exceeds GEMV_STATIC_SCRATCH_FLOATS */
 };
 
 /* Kernel variants (gemv_config.variant). */
@@ -173,6 +194,12 @@ typedef struct gemv_config {
 /*
  * c = B @ a on the current device, asynchronously on `stream`.
  *
+ * Source: Case Studies, Case B "Background" (the operation and its shapes:
+ * B (n, k) row-major, a (k,)); the cached launch below is the remedy of
+ * Case B.4 "forward() Python Closure Overhead" (Fix: build once, call the
+ * built kernel) and Case E "Builder Function lru_cache" (Fix: cache the
+ * builder's result per shape), where rebuilding per call cost 11-200 ms.
+ *
  *  B      device pointer, n*k elements, row-major (row i starts at B + i*k).
  *         Must be 2-byte aligned; 16-byte alignment plus k % 8 == 0 selects
  *         the aligned-vector variant, anything else the general variant.
@@ -202,6 +229,10 @@ int gemv(const void *B, const void *a, void *c, int64_t n, int64_t k, int dtype,
 /*
  * As gemv(), with a configuration forced field by field (zero fields left
  * to the planner; `overlap` is taken as given, so 0 is a plain launch).
+ * Source: Case Studies, Case C "nsys Profiling with Autotune Contamination"
+ * (Fix: disable autotune and fix the best config, so a trace holds only
+ * steady-state launches of one configuration); grid_split > 1 is the
+ * split-K pass plus reduce pass whose times Case C adds together.
  * `forced` may be NULL (same as gemv()).  An impossible
  * configuration (e.g. the aligned variant for k % 8 != 0, W not in
  * {4, 8, 16}, Sw not dividing W) returns GEMV_ERR_CONFIG.  Forced
@@ -240,7 +271,14 @@ typedef struct gemv_epilogue {
 } gemv_epilogue;
 
 /*
- * GEMV over a row-strided B with a fused epilogue:
+ * GEMV over a row-strided B with a fused epilogue.  Source: the optimization
+ * guide, "Optimization Checklist" item 7 "Epilogue Fusion" (activation, bias
+ * and scaling applied in registers before the single write-back).  The row
+ * stride has no counterpart on the pages; it reads B in place where a caller
+ * holds a padded matrix (the DPLR pull request's review notes that a
+ * non-contiguous input read with assumed strides gives wrong results: here
+ * the stride is an explicit argument).
+ *
  *
  *     c[i] = act(alpha * sum_{j<k} B[i*ldb + j] * a[j] + beta * bias[i])
  *
@@ -260,6 +298,8 @@ int gemv_fused(const void *B, int64_t ldb, const void *a, void *c, int64_t n, in
  * the current device, for B with the given alignment (b_aligned16 != 0:
  * 16-byte aligned), and reserve the split-K workspace for `stream` if the
  * configuration needs one.  Optional; gemv() does the same lazily.
+ * Source: Case Studies, Case B.4 (Fix: compile once at init time, so the
+ * call itself only launches) and Case E (Fix: cache per shape).
  */
 int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cudaStream_t stream);
 
@@ -267,40 +307,64 @@ int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cudaStream_t 
  * The planner as a pure host function (no CUDA call): the configuration
  * chosen for (n, k, dtype) on a device with `sm_count` SMs, for B with the
  * given alignment class, with `forced` fields (may be NULL) honoured.
- * Writes *out and returns GEMV_OK, or an error code.
+ * Writes *out and returns GEMV_OK, or an error code.  Source: Case Studies,
+ * Case E (the builder as a pure function of its shape parameters, which is
+ * what makes its result cacheable) and Case C "Why 74% and Not Higher"
+ * (occupancy set by n over the SM count; here the planner sizes the grid
+ * and the split for 152 SMs).
  */
 int gemv_plan(int64_t n, int64_t k, int dtype, int b_aligned16, int sm_count,
               const gemv_config *forced, gemv_config *out);
 
-/* The configuration of this thread's last successful gemv/gemv_ex launch. */
+/*
+ * The configuration of this thread's last successful gemv/gemv_ex/
+ * gemv_fused/gemv_splitk_noalloc launch.  Source: Case Studies, Case C (a
+ * profile is only readable against the one configuration that ran).
+ */
 int gemv_last_config(gemv_config *out);
 
-/* Static description of a status code (never NULL). */
+/*
+ * Static description of a status code (never NULL).  No counterpart on the
+ * pages, which raise Python exceptions; this ABI returns codes instead.
+ */
 const char *gemv_status_string(int status);
 
-/* The cudaError_t value behind this thread's last GEMV_ERR_CUDA (0 if none). */
+/*
+ * The cudaError_t value behind this thread's last GEMV_ERR_CUDA (0 if
+ * none).  No counterpart on the pages (see gemv_status_string).
+ */
 int gemv_last_cuda_error(void);
 
 /*
  * Test hook: the next gemv/gemv_ex/gemv_host call on any thread returns
  * `status` without launching anything (0 clears it).  Host-side only; no
- * GPU fault is ever involved.
+ * GPU fault is ever involved.  No counterpart on the pages: it makes every
+ * failure path of a caller testable without faulting a GPU.
  */
 int gemv_debug_inject(int status);
 
 /*
- * Waits of the bulk variant that gave up.  Each wait of a warp on one of its
+ * Waits of the bulk variant that gave up (the bulk variant is the sm_103a
+ * form of Case Studies, Case B.1 "O3 Pipelined B Loads"; its bounded waits
+ * have no counterpart on the pages).  Each wait of a warp on one of its
  * ring buffers polls the buffer's mbarrier a bounded number of times (2^20);
  * a warp whose wait runs out stops issuing copies, waits (again bounded) for
  * the copies it already issued, writes NaN for the rows it owns and adds one
  * to a per-device counter.  This reads that counter for the current device
  * into *count (synchronously: it waits for the device's outstanding work),
- * then zeroes it if `reset` is nonzero.
+ * then zeroes it if `reset` is nonzero.  Bits 0-30 of *count hold the
+ * number of warps that gave up.  Bit 31 (GEMV_DRAIN_TIMEOUT) is set if a
+ * warp's bounded wait for the copies it had already issued also ran out:
+ * its CTA then exited with a bulk copy possibly still writing shared
+ * memory, and the device's state is unspecified -- treat the device as
+ * unusable for the rest of the process.
  */
+#define GEMV_DRAIN_TIMEOUT 0x80000000u
 int gemv_wait_timeouts(int reset, uint32_t *count);
 
 /*
- * Test hook: the next launch of the bulk variant (on any thread) gives each
+ * Test hook (no counterpart on the pages): the next launch of the bulk
+ * variant (on any thread) gives each
  * ring wait `polls` polls instead of 2^20 (0 = every wait gives up at once,
  * exercising the path above without any hang); -1 clears it.  The waits
  * that drain copies already issued keep the full limit.
@@ -310,11 +374,14 @@ int gemv_debug_wait_budget(int32_t polls);
 /*
  * Free the library-owned workspaces and drop the configuration cache.  The
  * caller must make sure no call that uses them is still running on the GPU.
+ * Source: the inverse of the per-shape cache of Case Studies, Case E (whose
+ * lru_cache is bounded; this one is emptied explicitly).
  */
 int gemv_release(void);
 
 /*
- * End-to-end call for a matrix and vector held in host memory: copies B
+ * End-to-end call for a matrix and vector held in host memory (no
+ * counterpart on the pages, whose inputs are device tensors): copies B
  * (n*k elements) and a (k elements) from host to the caller's device buffers
  * B_dev and a_dev, runs gemv() into c_dev, and copies c back to c_host, all
  * asynchronously on `stream` (cudaMemcpyAsync; pinned host buffers make the
@@ -323,15 +390,6 @@ int gemv_release(void);
  */
 int gemv_host(const void *B_host, const void *a_host, void *c_host, void *B_dev, void *a_dev,
               void *c_dev, int64_t n, int64_t k, int dtype, cudaStream_t stream);
-
-/*
- * Measurement helper, not part of the product: a read-only streaming pass
- * over `bytes` bytes at `buf` (16-byte aligned, bytes % 16 == 0) with the
- * same load path as the GEMV kernels, to calibrate the achievable HBM read
- * bandwidth.  Writes one 32-bit checksum word per CTA to `sink` (device
- * memory of at least 64 KiB).  Asynchronous on `stream`.
- */
-int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t stream);
 
 /* Capacity, in floats, of the static split-K scratch of gemv_splitk_noalloc(). */
 #define GEMV_STATIC_SCRATCH_FLOATS (1 << 20) /* 4 MiB per GPU */
@@ -346,13 +404,18 @@ int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t str
  *
  * Computes the same c = B @ a as gemv() (same arguments, same status codes,
  * asynchronous on `stream`) with the tiles kernel split into `grid_split`
- * k-segments (2 .. 64; a k too short for that many segments of 8 columns uses
- * fewer, down to one), followed by the second pass that adds the fp32
- * partials in segment order.  The partials live in a file-scope device array
- * of GEMV_STATIC_SCRATCH_FLOATS floats that every GPU loading this library
- * holds until the process exits; a call needing more than that
- * (grid_split * n floats) returns GEMV_ERR_SCRATCH without launching.  No
- * cudaMalloc, cudaFree or other allocating routine is called.
+ * k-segments (2 .. 64), followed by the second pass that adds the fp32
+ * partials in segment order.  The split actually used can differ from the
+ * one requested: a k too short for that many segments of 8 columns uses
+ * fewer, down to one (k <= 8), and a row longer than grid_split * 32768
+ * columns uses ceil(k / 32768) segments (one segment stages at most 32768
+ * columns of a).  The partials live in a file-scope device array of
+ * GEMV_STATIC_SCRATCH_FLOATS floats that every GPU loading this library
+ * holds until the process exits; a call whose split needs more than that
+ * (segments * n floats, with two or more segments) returns GEMV_ERR_SCRATCH
+ * without launching.  A single segment writes c directly and uses no
+ * scratch, whatever n is.  No cudaMalloc, cudaFree or other allocating
+ * routine is called.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
@@ -420,6 +483,10 @@ enum {
 };
 
 /*
+ * Source: Case Studies, Case D "Background" (the same recurrence as
+ * gla_decode()).  The layouts are this library's own: the page's decode
+ * kernel is a warpgroup tensor-core pipeline, not a bandwidth-bound stream.
+ *
  * gla_decode() with the kernel layout chosen by the caller (`variant`,
  * GLA_VARIANT_*) and launch flags (`flags`, GLA_PREFETCH_STATE or 0;
  * unknown bits return GEMV_ERR_ARG).  The automatic choice is GLA_VARIANT_PIPE

@@ -11,7 +11,7 @@ built, every call raises.
 Names follow the C entry points: ``gemv``, ``gemv_ex``, ``gemv_fused``, ``gemv_prepare``,
 ``gemv_plan``, ``gemv_last_config``, ``gemv_status_string``,
 ``gemv_last_cuda_error``, ``gemv_debug_inject``, ``gemv_release``,
-``gemv_host``, ``gemv_probe_read``, ``gemv_splitk_noalloc``, ``gemv_wait_timeouts``,
+``gemv_host``, ``gemv_splitk_noalloc``, ``gemv_wait_timeouts``,
 ``gemv_debug_wait_budget``, ``gla_decode``, ``gla_decode_ex``.
 """
 from __future__ import annotations
@@ -30,6 +30,7 @@ GEMV_ERR_ARG, GEMV_ERR_DTYPE, GEMV_ERR_ALIAS, GEMV_ERR_DEVICE = -1, -2, -3, -4
 GEMV_ERR_CUDA, GEMV_ERR_CONFIG, GEMV_ERR_ALIGN, GEMV_ERR_NOMEM = -5, -6, -7, -8
 GEMV_ERR_SCRATCH = -9
 GEMV_STATIC_SCRATCH_FLOATS = 1 << 20
+GEMV_DRAIN_TIMEOUT = 0x80000000  # bit of gemv_wait_timeouts(): a drain of issued copies ran out
 GEMV_VARIANT_AUTO, GEMV_VARIANT_ROWS, GEMV_VARIANT_ROWS_GENERAL, GEMV_VARIANT_TILES = 0, 1, 2, 3
 GEMV_VARIANT_BULK = 4
 GEMV_OVERLAP_NONE, GEMV_OVERLAP_PDL, GEMV_OVERLAP_PDL_PREFETCH_B, GEMV_OVERLAP_PDL_PREFETCH_BA = 0, 1, 2, 3
@@ -44,7 +45,7 @@ ACTIVATIONS = {"none": GEMV_ACT_NONE, "relu": GEMV_ACT_RELU, "sigmoid": GEMV_ACT
 #: the C ABI's exported entry points (checked against include/gemv.h by the tests)
 ENTRY_POINTS = ("gemv", "gemv_ex", "gemv_fused", "gemv_prepare", "gemv_plan", "gemv_last_config",
                 "gemv_status_string", "gemv_last_cuda_error", "gemv_debug_inject",
-                "gemv_release", "gemv_host", "gemv_probe_read", "gemv_splitk_noalloc",
+                "gemv_release", "gemv_host", "gemv_splitk_noalloc",
                 "gemv_wait_timeouts", "gemv_debug_wait_budget", "gla_decode", "gla_decode_ex")
 
 
@@ -108,7 +109,6 @@ def lib() -> ctypes.CDLL:
             L.gemv_debug_inject.argtypes = [i32]
             L.gemv_release.argtypes = []
             L.gemv_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
-            L.gemv_probe_read.argtypes = [vp, i64, vp, vp]
             L.gemv_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
             L.gemv_wait_timeouts.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32)]
             L.gemv_debug_wait_budget.argtypes = [ctypes.c_int32]
@@ -305,16 +305,6 @@ def gemv_host(B_host: torch.Tensor, a_host: torch.Tensor, c_host: torch.Tensor, 
                              dtype_code(B_host.dtype, out_fp32), _stream_handle(stream))
     _check(st, "gemv_host")
     return c_host
-
-
-def gemv_probe_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
-    """Read-only bandwidth probe over ``buf`` (a measurement helper)."""
-    nbytes = buf.numel() * buf.element_size()
-    if sink.numel() * sink.element_size() < 65536:
-        raise ValueError("sink must hold at least 64 KiB")
-    with torch.cuda.device(buf.device):
-        st = lib().gemv_probe_read(buf.data_ptr(), nbytes, sink.data_ptr(), _stream_handle(stream))
-    _check(st, "gemv_probe_read")
 
 
 def gemv_splitk_noalloc(B, a, c=None, out_fp32: bool = False, grid_split: int = 2, stream=None) -> torch.Tensor:

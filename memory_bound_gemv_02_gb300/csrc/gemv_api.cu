@@ -12,6 +12,8 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -41,7 +43,6 @@ constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int64_t kSmemReservedPerCta = 1024;
 constexpr int kMaxDevices = 64;
 constexpr int kReduceThreads = 256;
-constexpr int kProbeSinkWords = 16384;  // 64 KiB
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -140,6 +141,28 @@ const DeviceInfo &device_info_locked(int dev) {
     }
   }
   return d;
+}
+
+// GEMV_LOG=1 in the environment (read once, at the first configuration
+// built): one line on stderr for each launch configuration the planner
+// builds -- a new key cached by gemv()/gemv_ex()/gemv_fused()/
+// gemv_prepare(), or a gemv_plan() call -- giving the key and what it maps
+// to.  Off otherwise.
+bool log_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("GEMV_LOG");
+    return v != nullptr && v[0] == '1' && v[1] == '\0';
+  }();
+  return on;
+}
+
+void log_config(const char *what, int dev, int64_t n, int64_t k, int dtype, bool aligned, const gemv_config &c) {
+  if (!log_enabled()) return;
+  std::fprintf(stderr,
+               "gemv: %s dev=%d n=%lld k=%lld dtype=%d aligned=%d -> variant=%d ctas=%d warps_per_cta=%d "
+               "warp_split=%d rows_per_warp=%d unroll=%d grid_split=%d k_segment=%lld stages=%d smem_bytes=%d\n",
+               what, dev, (long long)n, (long long)k, dtype, aligned ? 1 : 0, c.variant, c.ctas, c.warps_per_cta,
+               c.warp_split, c.rows_per_warp, c.unroll, c.grid_split, (long long)c.k_segment, c.stages, c.smem_bytes);
 }
 
 bool valid_W(int W) { return W == 4 || W == 8 || W == 16; }
@@ -648,6 +671,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
     cudaGetLastError();
     return GEMV_ERR_DEVICE;
   }
+  if (!on_device(dev, {k > 0 ? B : nullptr, k > 0 ? a : nullptr, c, ep.bias})) return GEMV_ERR_DEVICE;
   if (k == 0) {
     // The empty sum: +0 in every output format is all-zero bits; with an
     // epilogue, its value on 0 (the second-pass kernel over no partials).
@@ -697,6 +721,7 @@ int run_ld(const void *B, int64_t ldb, const void *a, void *c, int64_t n, int64_
         st = plan_impl(n, k, dtype, aligned, di.sm_count, nullptr, &cfg);
         if (st != GEMV_OK) return st;
         g_cache.emplace(key, cfg);
+        log_config("new config", dev, n, k, dtype, aligned, cfg);
       }
     }
     launch_smem = cfg.smem_bytes;
@@ -824,7 +849,9 @@ extern "C" int gemv_plan(int64_t n, int64_t k, int dtype, int b_aligned16, int s
                          const gemv_config *forced, gemv_config *out) {
   if (out == nullptr) return GEMV_ERR_ARG;
   const bool aligned = b_aligned16 != 0 && k % 8 == 0;
-  return plan_impl(n, k, dtype, aligned, sm_count, forced, out);
+  const int st = plan_impl(n, k, dtype, aligned, sm_count, forced, out);
+  if (st == GEMV_OK) log_config("plan", -1, n, k, dtype, aligned, *out);
+  return st;
 }
 
 extern "C" int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cudaStream_t stream) {
@@ -849,6 +876,7 @@ extern "C" int gemv_prepare(int64_t n, int64_t k, int dtype, int b_aligned16, cu
     int st = plan_impl(n, k, dtype, aligned, di.sm_count, nullptr, &cfg);
     if (st != GEMV_OK) return st;
     g_cache.emplace(key, cfg);
+    log_config("new config", dev, n, k, dtype, aligned, cfg);
   }
   MainKernel mk = lookup_main(dtype, cfg, aligned);
   if (mk == nullptr) return GEMV_ERR_CONFIG;
@@ -874,12 +902,13 @@ extern "C" const char *gemv_status_string(int status) {
     case GEMV_ERR_ARG: return "invalid argument (null pointer, negative or oversized n/k)";
     case GEMV_ERR_DTYPE: return "unknown dtype code";
     case GEMV_ERR_ALIAS: return "output c overlaps input B or a";
-    case GEMV_ERR_DEVICE: return "no usable device (current device must be sm_103)";
+    case GEMV_ERR_DEVICE:
+      return "no usable device (current device must be sm_103), or a buffer not in the current device's memory";
     case GEMV_ERR_CUDA: return "a CUDA call or kernel launch failed (see gemv_last_cuda_error)";
     case GEMV_ERR_CONFIG: return "configuration invalid for this shape";
     case GEMV_ERR_ALIGN: return "pointer not aligned to its element type";
     case GEMV_ERR_NOMEM: return "split-K workspace allocation failed";
-    case GEMV_ERR_SCRATCH: return "split-K scratch needed (grid_split * n floats) exceeds the static scratch array";
+    case GEMV_ERR_SCRATCH: return "split-K scratch needed (segments * n floats) exceeds the static scratch array";
     default: return "unknown status";
   }
 }
@@ -943,7 +972,13 @@ extern "C" int gemv_host(const void *B_host, const void *a_host, void *c_host, v
   if (st != GEMV_OK) return st;
   if (n == 0) return GEMV_OK;
   if (c_host == nullptr || (k > 0 && (B_host == nullptr || a_host == nullptr))) return GEMV_ERR_ARG;
-  cudaError_t e;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMV_ERR_DEVICE;
+  }
+  if (!on_device(dev, {k > 0 ? B_dev : nullptr, k > 0 ? a_dev : nullptr, c_dev})) return GEMV_ERR_DEVICE;
   if (k > 0) {
     e = cudaMemcpyAsync(B_dev, B_host, (size_t)n * (size_t)k * 2, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -953,33 +988,6 @@ extern "C" int gemv_host(const void *B_host, const void *a_host, void *c_host, v
   st = run(B_dev, a_dev, c_dev, n, k, dtype, nullptr, stream);
   if (st != GEMV_OK) return st;
   e = cudaMemcpyAsync(c_host, c_dev, (size_t)n * out_elem_bytes(dtype), cudaMemcpyDeviceToHost, stream);
-  if (e != cudaSuccess) return cuda_fail(e);
-  return GEMV_OK;
-}
-
-extern "C" int gemv_probe_read(const void *buf, int64_t bytes, void *sink, cudaStream_t stream) {
-  if (buf == nullptr || sink == nullptr || bytes <= 0) return GEMV_ERR_ARG;
-  if (((uintptr_t)buf & 15u) || (bytes & 15) || ((uintptr_t)sink & 3u)) return GEMV_ERR_ALIGN;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return GEMV_ERR_DEVICE;
-  }
-  int sms;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    const DeviceInfo &di = device_info_locked(dev);
-    if (!di.ok) return GEMV_ERR_DEVICE;
-    sms = di.sm_count;
-  }
-  ProbeKernel pk = probe_kernel();
-  int per_sm = 0;
-  cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void *)pk, 512, 0);
-  if (oe != cudaSuccess) return cuda_fail(oe);
-  int grid = sms * (per_sm > 0 ? per_sm : 1);
-  if (grid > kProbeSinkWords) grid = kProbeSinkWords;
-  pk<<<grid, 512, 0, stream>>>(static_cast<const uint4 *>(buf), bytes / 16, static_cast<uint32_t *>(sink));
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return GEMV_OK;
 }
@@ -1036,6 +1044,7 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
     cudaGetLastError();
     return GEMV_ERR_DEVICE;
   }
+  if (!on_device(dev, {k > 0 ? B : nullptr, k > 0 ? a : nullptr, c})) return GEMV_ERR_DEVICE;
   if (k == 0) {
     e = cudaMemsetAsync(c, 0, (size_t)n * out_elem_bytes(dtype), stream);
     return e == cudaSuccess ? GEMV_OK : cuda_fail(e);
@@ -1049,7 +1058,10 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
     if (!di.ok) return GEMV_ERR_DEVICE;
     gemv_config forced{};
     forced.variant = GEMV_VARIANT_TILES;
-    forced.grid_split = grid_split;
+    // A segment stages at most kMaxSegment columns of a: longer rows take
+    // as many segments as that needs, even beyond the requested split.
+    const int64_t need = cdiv(k, kMaxSegment);
+    forced.grid_split = (int32_t)(need > grid_split ? need : grid_split);
     st = plan_impl(n, k, dtype, aligned, di.sm_count, &forced, &cfg);
     if (st != GEMV_OK) return st;
     if (cfg.smem_bytes > di.max_smem_optin) return GEMV_ERR_CONFIG;
@@ -1058,8 +1070,11 @@ extern "C" int gemv_splitk_noalloc(const void *B, const void *a, void *c, int64_
     e = ensure_smem_attr_locked((const void *)mk, dev, cfg.smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  // A short k can leave a single segment (no scratch needed at all).
-  if ((int64_t)cfg.grid_split * n > (int64_t)GEMV_STATIC_SCRATCH_FLOATS) return GEMV_ERR_SCRATCH;
+  // Only a plan of two or more segments keeps partials in the scratch; a
+  // short k can leave a single segment, which writes c directly and needs
+  // no scratch whatever n is.
+  if (cfg.grid_split > 1 && (int64_t)cfg.grid_split * n > (int64_t)GEMV_STATIC_SCRATCH_FLOATS)
+    return GEMV_ERR_SCRATCH;
   float *ws = nullptr;
   if (cfg.grid_split > 1) {
     st = static_scratch_for(dev, &ws);

@@ -2,7 +2,10 @@
 // units of the GEMV library.  Not installed; the public surface is gemv.h.
 #pragma once
 
+#include <cuda_runtime_api.h>
 #include <stdint.h>
+
+#include <initializer_list>
 
 #ifdef __CUDACC__
 #define GEMV_HD __host__ __device__
@@ -49,7 +52,6 @@ struct Params {
 
 typedef void (*MainKernel)(Params);
 typedef void (*ReduceKernel)(const float *, void *, int64_t, int32_t, Epilogue);
-typedef void (*ProbeKernel)(const uint4 *, int64_t, uint32_t *);
 
 // Kernel lookup.  in16: 0 fp16, 1 bf16.  out_f32: 0 same as input, 1 fp32.
 // variant: 1 aligned rows, 2 general rows.  R: rows per warp.
@@ -67,7 +69,25 @@ MainKernel bulk_kernel_f16(int out_f32, int aligned, int U, int epi);
 MainKernel bulk_kernel_bf16(int out_f32, int aligned, int U, int epi);
 ReduceKernel reduce_kernel_f16(int out_f32);
 ReduceKernel reduce_kernel_bf16(int out_f32);
-ProbeKernel probe_kernel();
+
+// Where a caller's buffer lives: every non-null pointer must start in
+// device memory of `dev` (the current device) or in managed memory, which
+// every device reaches.  Host memory (pinned, registered or pageable) and
+// another device's memory give false.  One cudaPointerGetAttributes per
+// pointer, no allocation, nothing launched.
+inline bool on_device(int dev, std::initializer_list<const void *> ptrs) {
+  for (const void *q : ptrs) {
+    if (q == nullptr) continue;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (at.type == cudaMemoryTypeManaged) continue;
+    if (at.type != cudaMemoryTypeDevice || at.device != dev) return false;
+  }
+  return true;
+}
 
 // Loads per lane issued back to back (per row) for R rows per warp.
 inline int unroll_for_rows(int R) { return R == 1 ? 8 : (R == 2 ? 4 : 2); }
@@ -81,6 +101,7 @@ constexpr int kFlagDeferStores = 32;  // tiles kernel with kFlagPrefetchA: keep 
 constexpr int kFlagL2First = 64;      // without kFlagPrefetchB: ask L2 for the first tile of B before the wait
 constexpr int64_t kDeferMaxRows = 4096;  // most rows per CTA whose results are kept (16 KB of shared memory)
 constexpr int kWaitPolls = 1 << 20;  // default bound on the polls of one mbarrier wait
+constexpr uint32_t kDrainTimeoutBit = 0x80000000u;  // timeout counter: a drain of issued copies ran out
 
 // Shared-memory layout of the bulk kernel, in bytes from the start of the
 // dynamic allocation: staged a (as_elems * 2), slice partials (2 * W

@@ -593,6 +593,9 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
     return GEMV_ERR_DEVICE;
   }
   if (major != 10 || minor != 3) return GEMV_ERR_DEVICE;
+  if (!on_device(dev, {dk > 0 ? q : nullptr, dk > 0 ? k : nullptr, v, dk > 0 ? gk : nullptr,
+                       dk > 0 ? S : nullptr, dk > 0 ? S_new : nullptr, o}))
+    return GEMV_ERR_DEVICE;
   const int cpr = (int)(dv / VEC);
   // The pipelined CTA layout needs q, k, gk rows of whole 16-byte chunks and
   // a round (G heads, G >= 1) of at most kGlaPipeRoundChunks state chunks.

@@ -85,13 +85,6 @@ def test_debug_inject_is_one_shot(gemv_lib):
         gemv_lib.GEMV_ERR_NOMEM
 
 
-def test_probe_argument_checks(gemv_lib):
-    L = gemv_lib.lib()
-    assert L.gemv_probe_read(None, 16, C_ADDR, None) == gemv_lib.GEMV_ERR_ARG
-    assert L.gemv_probe_read(B_ADDR + 8, 16, C_ADDR, None) == gemv_lib.GEMV_ERR_ALIGN
-    assert L.gemv_probe_read(B_ADDR, 17, C_ADDR, None) == gemv_lib.GEMV_ERR_ALIGN
-
-
 def test_config_struct_layout_matches_header(gemv_lib):
     # int32 x 8, int64, int32 x 2, int32[4]  ->  8*4 + 8 + 2*4 + 16 = 64 bytes
     assert ctypes.sizeof(gemv_lib.GemvConfig) == 64

@@ -9,13 +9,20 @@ fixed device array of the library instead of allocated memory.  Its output
 must match the existing gemv() entry point's within the tolerances the other
 tests use (1e-2 * max(1, |c|) for 16-bit output, 1e-5 * sum_j |B_ij a_j| for
 fp32 output), on two calls in a row, and it must refuse, without launching, a
-call whose partials would not fit in the array.
+call whose partials would not fit in the array.  A call whose plan keeps a
+single segment (k <= 8) writes c directly and needs no scratch however many
+rows it has; a row longer than the requested split can stage takes more
+segments.  And the call must not allocate: free device memory stays the same
+across calls on streams the library has never seen, while the allocating
+split-K path of gemv_ex() on such a stream visibly takes its workspace.
 
 The file name makes pytest collect it last, so that a run stopping at the
 first failure has already run every other test; it also passes alone in a
 fresh process (its first call sets the scratch address up).
 """
 from __future__ import annotations
+
+import ctypes
 
 import numpy as np
 import pytest
@@ -104,3 +111,70 @@ def test_oversized_call_is_refused_without_launching(cuda_dev):
     assert _noalloc(B[:n2], a, c2, False, 2) == g.GEMV_OK
     torch.cuda.synchronize()
     _matches_gemv(c2, B[:n2], a, False, "largest fitting call")
+
+
+def test_single_segment_needs_no_scratch(cuda_dev):
+    # k = 8 leaves one segment whatever split is asked for: c is written
+    # directly, so more rows than the scratch holds floats are fine
+    n, k = g.GEMV_STATIC_SCRATCH_FLOATS + 1, 8
+    B, a = inputs.make_inputs(n, k, "f16", "uniform", 5, cuda_dev)
+    for out_fp32 in (False, True):
+        c = torch.full((n,), 9.0, dtype=torch.float32 if out_fp32 else torch.float16, device=cuda_dev)
+        assert _noalloc(B, a, c, out_fp32, 4) == g.GEMV_OK
+        torch.cuda.synchronize()
+        assert g.gemv_last_config()["grid_split"] == 1
+        check_against_oracle(c, B, a, out_fp32, label=f"one segment, {n} rows")
+        _matches_gemv(c, B, a, out_fp32, "one segment")
+
+
+def test_long_rows_take_the_segments_they_need(cuda_dev):
+    # 3 * 32768 + 5 columns need 4 segments of at most 32768; a split of 2
+    # is raised to that
+    n, k = 6, 3 * 32768 + 5
+    B, a = inputs.make_inputs(n, k, "bf16", "uniform", 6, cuda_dev)
+    for _ in range(2):
+        c = torch.empty(n, dtype=torch.float32, device=cuda_dev)
+        assert _noalloc(B, a, c, True, 2) == g.GEMV_OK
+        torch.cuda.synchronize()
+        assert g.gemv_last_config()["grid_split"] == 4
+        check_against_oracle(c, B, a, True, label="long rows")
+        _matches_gemv(c, B, a, True, "long rows")
+
+
+def test_no_device_memory_is_allocated(cuda_dev):
+    """Free device memory (cudaMemGetInfo) is unchanged across calls on a
+    stream the library has never seen; as a control, the allocating split-K
+    path (gemv_ex with the same split) on another new stream takes its
+    workspace of grid_split * n floats (4 MiB here) and free memory drops."""
+    n, k, split = 65536, 4096, 16  # 16 * 65536 floats: the whole scratch array
+    B, a = inputs.make_inputs(n, k, "f16", "uniform", 7, cuda_dev)
+    c = torch.empty(n, dtype=torch.float16, device=cuda_dev)
+    c_ctl = torch.empty(n, dtype=torch.float16, device=cuda_dev)
+    # The first call on the device looks the scratch address up and loads
+    # the kernels (lazy module loading maps their code into device memory).
+    assert _noalloc(B, a, c, False, split) == g.GEMV_OK
+    torch.cuda.synchronize()
+    s_new, s_ctl = torch.cuda.Stream(), torch.cuda.Stream()
+    for st in (s_new, s_ctl):  # one ordinary launch on each new stream first
+        with torch.cuda.stream(st):
+            c.zero_()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    L = g.lib()
+    for _ in range(3):
+        assert L.gemv_splitk_noalloc(B.data_ptr(), a.data_ptr(), c.data_ptr(), n, k, g.GEMV_F16, split,
+                                     s_new.cuda_stream) == g.GEMV_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes across allocation-free calls"
+    check_against_oracle(c, B, a, False, label="calls on a new stream")
+    cfg = g.GemvConfig()
+    cfg.variant = g.GEMV_VARIANT_TILES
+    cfg.grid_split = split
+    cfg.overlap = g.GEMV_OVERLAP_NONE
+    assert L.gemv_ex(B.data_ptr(), a.data_ptr(), c_ctl.data_ptr(), n, k, g.GEMV_F16, ctypes.byref(cfg),
+                     s_ctl.cuda_stream) == g.GEMV_OK
+    torch.cuda.synchronize()
+    free2, _ = torch.cuda.mem_get_info()
+    assert free0 - free2 >= split * n * 4, "control: the allocating path's workspace should show"
+    assert torch.equal(c_ctl, c)  # same plan, same kernels: bit-identical
