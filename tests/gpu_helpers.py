@@ -24,10 +24,32 @@ def sample_rows(n: int, m: int = 192, seed: int = 0) -> np.ndarray:
     return np.unique(np.concatenate([np.arange(edge), np.arange(n - edge, n), mid]))
 
 
+def oracle_chunked(B_bits: np.ndarray, a_bits: np.ndarray, fmt: str, chunk_rows: int = 2048):
+    """The oracle over every row of ``B_bits``, row chunks run on a pool of
+    host threads (each chunk is one unchanged oracle call; rows are
+    independent, so the result equals one call over the whole matrix)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    n = B_bits.shape[0]
+    c = np.empty(n, dtype=np.float64)
+    s = np.empty(n, dtype=np.float64)
+
+    def one(i0):
+        ci, si = oracle.gemv_ref(B_bits[i0:i0 + chunk_rows], a_bits, fmt)
+        c[i0:i0 + chunk_rows] = ci
+        s[i0:i0 + chunk_rows] = si
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(one, range(0, n, chunk_rows)))
+    return c, s
+
+
 def oracle_for(B: torch.Tensor, a: torch.Tensor, rows=None):
     fmt = fmt_of(B)
     a_bits = inputs.to_bits(a)
     if rows is None:
+        if B.numel() >= (1 << 26):  # large: rows in parallel chunks
+            return oracle_chunked(inputs.to_bits(B), a_bits, fmt)
         return oracle.gemv_ref(inputs.to_bits(B), a_bits, fmt)
     idx = torch.as_tensor(np.asarray(rows), device=B.device, dtype=torch.long)
     return oracle.gemv_ref(inputs.to_bits(B.index_select(0, idx)), a_bits, fmt)
