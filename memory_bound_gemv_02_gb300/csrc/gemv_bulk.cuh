@@ -236,13 +236,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_bulk_kernel(const Params 
   }
   if (bad && lane == 0) {
     // Copies issued but not consumed, [cfail, ic), one per buffer at most:
-    // wait for each (bounded) before the CTA's shared memory goes away.
+    // wait for each (bounded) before the CTA's shared memory goes away.  If
+    // one of these waits runs out too, a copy may still be in flight when
+    // the CTA exits: that is recorded apart, in the counter's top bit.
     int b = fb;
+    bool drained = true;
     for (int64_t j = cfail; j < ic; ++j) {
-      ring_wait(&bars[b], (uint32_t)((j / NS) & 1), kWaitPolls);
+      if (!ring_wait(&bars[b], (uint32_t)((j / NS) & 1), kWaitPolls)) drained = false;
       if (++b == NS) b = 0;
     }
     atomicAdd(p.timeouts, 1u);
+    if (!drained) atomicOr(p.timeouts, kDrainTimeoutBit);
   }
 }
 
