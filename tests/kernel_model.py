@@ -482,7 +482,7 @@ GLA_PIPE_MAX_SMEM = 110 * 1024
 def gla_pipe_smem(G, dk, dv, elem_bytes, threads=256):
     cpr = dv * elem_bytes // 16
     RP = threads // G // cpr
-    return 2 * 16 * (G * dk * cpr + 3 * (G * dk * elem_bytes // 16) + G * cpr) + 4 * G * RP * dv
+    return 2 * 16 * (G * dk * cpr + 3 * (G * dk * elem_bytes // 16) + G * cpr) + 4 * G * RP * dv + 3 * 4 * G * dk
 
 
 def gla_pipe_ok(dk, dv, elem_bytes):
@@ -527,7 +527,9 @@ def replay_gla_pipe(bh, dk, dv, elem_bytes, threads=256, grid=None):
     assert RP >= 1 and G * dk * cpr <= GLA_PIPE_ROUND_CHUNKS
     SC, QC = G * dk * cpr, G * dk * elem_bytes // 16
     BUF = SC + 3 * QC + G * cpr
-    smem = 2 * BUF * 16 + G * RP * dv * 4
+    PARTS = 2 * BUF * 16                    # byte offset of o's partials
+    FACT = PARTS + G * RP * dv * 4          # byte offset of the fp32 exp(gk), k, q
+    smem = FACT + 3 * G * dk * 4
     assert smem == gla_pipe_smem(G, dk, dv, elem_bytes, threads) <= GLA_PIPE_MAX_SMEM
     rounds = -(-bh // G)
     grid = rounds if grid is None else min(grid, rounds)
@@ -586,6 +588,17 @@ def replay_gla_pipe(bh, dk, dv, elem_bytes, threads=256, grid=None):
                     v_copied[src] += 1
             h0 = r * G
             nh = min(G, bh - h0)
+            # the fp32 factors: element x of exp(gk), k and q (x < nh * dk,
+            # written by thread x % threads) from the buffer's q, k, gk chunks
+            converted = set()
+            for t in range(threads):
+                for x in range(t, nh * dk, threads):
+                    for a in range(3):
+                        qsm = b * BUF + SC + a * QC + (x * elem_bytes) // 16
+                        assert cur[qsm][0] == "qkg"[a]
+                        off = FACT + 4 * (a * G * dk + x)
+                        assert FACT <= off and off + 4 <= smem
+                    converted.add(x)
             for t in range(threads):
                 gi, tl = divmod(t, TPG)
                 cc, rl = tl % cpr, tl // cpr
@@ -599,13 +612,14 @@ def replay_gla_pipe(bh, dk, dv, elem_bytes, threads=256, grid=None):
                     kind, src, owner = cur[sm]
                     assert kind == "S" and owner == t and src == (h * dk + i) * cpr + cc
                     read[src] += 1
-                    x = gi * dk + i  # element of q, k, gk in the buffer
+                    x = gi * dk + i  # element of q, k, gk in the buffer and of the fp32 factors
+                    assert x in converted
                     for a in range(3):
                         qsm = b * BUF + SC + a * QC + (x * elem_bytes) // 16
                         assert cur[qsm][0] == "qkg"[a]
                         assert cur[qsm][1] * 16 // elem_bytes + (x * elem_bytes % 16) // elem_bytes == h * dk + i
-                base = 2 * BUF * 16 + ((gi * RP + rl) * dv + cc * vec) * 4
-                assert base + 4 * vec <= smem and base % 16 == 0
+                base = PARTS + ((gi * RP + rl) * dv + cc * vec) * 4
+                assert base + 4 * vec <= FACT and base % 16 == 0
             for x in range(nh * dv):
                 g, jj = divmod(x, dv)
                 o_written[h0 + g, jj] += 1

@@ -167,7 +167,6 @@ def test_no_device_memory_is_allocated(cuda_dev):
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, f"free device memory changed by {free0 - free1} bytes across allocation-free calls"
-    check_against_oracle(c, B, a, False, label="calls on a new stream")
     cfg = g.GemvConfig()
     cfg.variant = g.GEMV_VARIANT_TILES
     cfg.grid_split = split
@@ -177,4 +176,6 @@ def test_no_device_memory_is_allocated(cuda_dev):
     torch.cuda.synchronize()
     free2, _ = torch.cuda.mem_get_info()
     assert free0 - free2 >= split * n * 4, "control: the allocating path's workspace should show"
+    # (checked only now: copying c to the host allocates through torch)
     assert torch.equal(c_ctl, c)  # same plan, same kernels: bit-identical
+    check_against_oracle(c, B, a, False, label="calls on a new stream")
