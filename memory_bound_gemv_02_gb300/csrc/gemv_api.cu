@@ -373,8 +373,18 @@ int plan_tiles(int64_t n, int64_t k, bool aligned, int sm, const gemv_config *f,
       C = (f->ctas / Sg) / NCLS * NCLS;
     } else {
       C = resident / Sg;
-      const int64_t need = groups * NCLS;  // CTAs that would have work
-      if (C > need) C = need;
+      const int64_t need = groups * NCLS;  // CTAs that would have work in whole tiles
+      // Rows are dealt to a class's CTAs one at a time, so a grid of every
+      // resident slot still gives each CTA rows, in one part-filled tile
+      // instead of fewer CTAs with full ones.  Kept for the tiles kernel
+      // when each CTA gets at least half a tile and rows are long: measured
+      // on GB300 as gemv() launches it, 1024 x 16384 f16 7.96 -> 7.74 us,
+      // 4099 x 7169 bf16 11.50 -> 11.32, 4099 x 4096 f16 7.25 -> 7.15,
+      // 4096 x 4096 bf16 7.16 -> 7.10, others within 0.5 %; at k = 1000 it
+      // was slower (4099 x 1000 3.38 -> 3.43, 1024 x 1000 2.81 -> 3.21).
+      const bool spread = !bulk && Sg == 1 && k >= 4096 && C / NCLS >= 1 &&
+                          rows_per_class * 2 >= RT * (C / NCLS);
+      if (C > need && !spread) C = need;
       C = C / NCLS * NCLS;
     }
     if (C < NCLS) C = NCLS;

@@ -55,7 +55,10 @@ def test_plan_shapes_of_interest(gemv_lib):
     p = gemv_lib.gemv_plan(14336, 4096, 1, True, SM)
     assert (p["warp_split"], p["rows_per_warp"], p["unroll"]) == (1, 1, 8)
     p = gemv_lib.gemv_plan(4096, 4096, 1, True, SM)
-    assert (p["warp_split"], p["rows_per_warp"], p["ctas"]) == (1, 1, 256)
+    assert (p["warp_split"], p["rows_per_warp"], p["ctas"]) == (1, 1, 304)  # every slot: part-filled tiles
+    assert gemv_lib.gemv_plan(4099, 1000, 0, True, SM)["ctas"] == 257        # short rows: whole tiles only
+    assert gemv_lib.gemv_plan(1024, 1000, 0, True, SM)["ctas"] == 64
+    assert gemv_lib.gemv_plan(4099, 7169, 1, False, SM)["ctas"] == 304
     p = gemv_lib.gemv_plan(1024, 4096, 0, True, SM)
     assert (p["warp_split"], p["unroll"]) == (4, 4)
     p = gemv_lib.gemv_plan(256, 512, 0, True, SM)
