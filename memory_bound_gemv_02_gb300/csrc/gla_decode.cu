@@ -66,6 +66,17 @@ struct GlaIo<F16> {
   static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
     static_cast<uint16_t *>(p)[i] = F16::from_float(x);
   }
+  // As pack(), rounding each pair with one paired conversion (the same
+  // nearest-even rounding of each element, hence the same bits).
+  static __device__ __forceinline__ uint4 pack_pairs(const float (&f)[VEC]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+      w[q] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
 };
 
 template <>
@@ -85,6 +96,15 @@ struct GlaIo<BF16> {
   static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
     static_cast<uint16_t *>(p)[i] = BF16::from_float(x);
   }
+  static __device__ __forceinline__ uint4 pack_pairs(const float (&f)[VEC]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+      w[q] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
 };
 
 template <>
@@ -102,6 +122,7 @@ struct GlaIo<F32> {
   static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
     static_cast<float *>(p)[i] = x;
   }
+  static __device__ __forceinline__ uint4 pack_pairs(const float (&f)[VEC]) { return pack(f); }
 };
 
 constexpr int kGlaThreads = 256;
@@ -305,6 +326,7 @@ __global__ void __launch_bounds__(kGlaThreads, 3) gla_decode_kernel_small(GlaPar
 // round's state (or, with GLA_PREFETCH_STATE, every thread already copies
 // its part of it): measured 3-8 % faster back to back.
 constexpr int kGlaPipeRoundChunks = 2048;
+constexpr int64_t kGlaPairPackMaxHead = 16 * 1024;  // state bytes of a head up to which S_new is stored through pack_pairs
 // Shared memory of one CTA at most: two CTAs per SM (228 KB, 1 KB reserved
 // per CTA).  More heads per round measured faster than more CTAs per SM:
 // 4096 x 64 x 64 fp16 13.8 us with 4 heads per round and 2 CTAs per SM
@@ -330,7 +352,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 // Wait until at most one committed group of this thread is still pending.
 __device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-template <class T>
+// PAIRS: store S_new through IO::pack_pairs (same bits).  Measured on GB300
+// back to back, it is faster for heads of at most kGlaPairPackMaxHead bytes
+// (4096 x 64 x 64 fp16 13.71 -> 12.59 us, 16384 x 16 x 64 fp16 16.51 ->
+// 15.47, 8192 x 64 x 64 bf16 22.50 -> 22.36) and slower for some larger ones
+// (4096 x 128 x 128 fp16 42.55 -> 44.00, bf16 42.08 -> 43.90).
+template <class T, bool PAIRS>
 __global__ void __launch_bounds__(kGlaThreads) gla_decode_pipe_kernel(GlaParams p) {
   using IO = GlaIo<T>;
   constexpr int VEC = IO::VEC;
@@ -442,7 +469,7 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_pipe_kernel(GlaParams 
           sn[e] = fmaf(di, s[e], ki * vv[e]);
           acc[e] = fmaf(qi, sn[e], acc[e]);
         }
-        stg_stream(Nrow + (int64_t)i * cpr, IO::pack(sn));
+        stg_stream(Nrow + (int64_t)i * cpr, PAIRS ? IO::pack_pairs(sn) : IO::pack(sn));
       }
       store_partials<VEC>(part, (gi * RP + rl) * dv + cc * VEC, acc);
     }
@@ -655,8 +682,10 @@ extern "C" int gla_decode_ex(const void *q, const void *k, const void *v, const 
       G *= 2;
     p.heads_per_cta = G;
     const size_t smem = (size_t)gla_pipe_smem(G, dk, dv, cpr, es);
-    void (*fn)(GlaParams) = dtype == GLA_F16 ? gla_decode_pipe_kernel<F16>
-                            : dtype == GLA_BF16 ? gla_decode_pipe_kernel<BF16> : gla_decode_pipe_kernel<F32>;
+    const bool pairs = dk * dv * es <= kGlaPairPackMaxHead;
+    void (*fn)(GlaParams) = dtype == GLA_F16    ? (pairs ? gla_decode_pipe_kernel<F16, true> : gla_decode_pipe_kernel<F16, false>)
+                            : dtype == GLA_BF16 ? (pairs ? gla_decode_pipe_kernel<BF16, true> : gla_decode_pipe_kernel<BF16, false>)
+                                                : gla_decode_pipe_kernel<F32, false>;
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute((const void *)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return GEMV_ERR_CUDA;
