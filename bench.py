@@ -879,7 +879,7 @@ def run_ours(args, world, rank, local):
         "probe_read_gbs": None if read_ceiling is None else round(read_ceiling, 1),
         "frac_of_read_ceiling": None if read_ceiling is None else round(achieved / read_ceiling, 4),
         "read_ceiling": None if native is None else {
-            "how": "read-only 16-byte streaming loads, back to back over two buffers, CUDA events after a "
+            "how": "read-only 32-byte streaming loads, back to back over two buffers, CUDA events after a "
                    "queue prefill; 'overlapped' = programmatic launches that never wait",
             "gbs_1gib_overlapped": native["read_gbs_1gib_overlapped"],
             "gbs_1gib_plain": native["read_gbs_1gib_plain"],
