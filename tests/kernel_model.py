@@ -368,6 +368,34 @@ def staged_shifted(a, j0, seglen, off, as_elems):
 
 
 
+def staging_schedule(nvec, block, shifted):
+    """Replay of the staging loop's thread schedule (``stage_shift_loop``):
+    unshifted, thread x of a ``block``-thread CTA first takes pairs
+    (q, q + block) for q = x, x + 2*block, ... while q + block < ``nvec``
+    (both loads before either store), then single vectors; shifted, single
+    vectors only.  Checks that every output vector is written exactly once
+    and every load address is inside [0, nvec).  Returns the largest number
+    of paired iterations of a thread."""
+    writes = np.zeros(nvec, dtype=np.int64)
+    most = 0
+    for x in range(block):
+        q = x
+        it = 0
+        if not shifted:
+            while q + block < nvec:
+                assert 0 <= q and q + block < nvec
+                writes[q] += 1
+                writes[q + block] += 1
+                q += 2 * block
+                it += 1
+        while q < nvec:
+            writes[q] += 1
+            q += block
+        most = max(most, it)
+    assert (writes == 1).all(), f"vectors written {writes.min()}..{writes.max()} times"
+    return most
+
+
 def gla_partial_store_conflicts(cpr, vec, dv):
     """Bank-conflict count of the GLA partial stores (``store_partials``):
     a warp's lanes (column chunk cc = lane % cpr, row block lane // cpr) each

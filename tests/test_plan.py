@@ -208,6 +208,17 @@ def test_shifted_staging_model(off, j0, seglen, k):
     assert (got == want).all()
 
 
+@pytest.mark.parametrize("shifted", [False, True])
+@pytest.mark.parametrize("block", [32, 256, 512, 1024])
+@pytest.mark.parametrize("nvec", [0, 1, 31, 32, 33, 255, 256, 257, 511, 512, 513, 1023, 1024, 1025, 1056, 2048, 2049,
+                                  2051, 4096, 4100])
+def test_staging_schedule(nvec, block, shifted):
+    """Every staged vector written exactly once by the paired-then-single
+    staging loop, and the pairs taken wherever a thread has two vectors."""
+    most = kernel_model.staging_schedule(nvec, block, shifted)
+    assert most == (0 if shifted or nvec <= block else -(-(nvec - block) // (2 * block)))
+
+
 @pytest.mark.parametrize("n,k,ldb", [(5, 17, 24), (9, 64, 72), (9, 64, 67), (33, 100, 100), (17, 7, 8), (3, 4099, 5000),
                                      (40, 256, 264), (7, 1000, 1003)])
 @pytest.mark.parametrize("base_off", [0, 3])
