@@ -220,15 +220,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     }
   };
 
-  // The first tile's first loads go out before a is staged, so the B
-  // stream starts at once and the staging latency hides under it.  Under a
-  // programmatic dependent launch with kFlagPrefetchB they even go out
-  // before the preceding kernel has finished (B is then promised read-only);
-  // a and c are touched only after wait_for_predecessor().  Without that
+  // Under a programmatic dependent launch with kFlagPrefetchB the first
+  // tile's first loads go out before the preceding kernel has finished (B
+  // is then promised read-only), and a is staged after them.  Without that
   // promise (kFlagL2First), each warp only asks L2 for the blocks of its
-  // first loads before waiting: a prefetch reads nothing into the kernel,
+  // first loads before waiting (a prefetch reads nothing into the kernel,
   // and L2 is where the preceding kernel's writes land, so no write can be
-  // missed.
+  // missed); after the wait a is staged first and the first loads, L2 hits
+  // by then, go out behind it.  a is read by every CTA at once; issued
+  // behind eight B loads per lane its loads queued for ~3 us after the
+  // wait, and staging it first measured 3-16 % faster per call back to back
+  // (7168 x 16384 33.0 -> 31.8 us, 4096 x 4096 7.10 -> 6.33), faster as
+  // plain and isolated launches too.  a and c are touched only after
+  // wait_for_predecessor().
   allow_dependents();
   const bool early = (p.flags & kFlagPrefetchB) != 0;
   if (!early) {
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
       prefetch_l2(bal + gb + t0, (uint32_t)nb * 16u);
     }
     wait_for_predecessor();
+    stage_a_shifted(p, as4, j0, len, off);
   }
   uint4 bv[U][R];
   bool prefetched = false;
@@ -249,10 +254,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     prefetched = true;
     // Also ask L2 for the blocks of the warp's second step (the next 32*U
     // blocks of its rows' slices), so that HBM keeps streaming while the
-    // CTA stages a.  With B promised unwritten this goes out before the
-    // wait on the predecessor; otherwise (issued after the wait, like the
-    // first step's loads) only when the CTA streams more than one row tile
-    // (4096 x 4096, a single tile per CTA, measured 6 % slower with it).
+    // first step is consumed.  With B promised unwritten this goes out
+    // before the wait on the predecessor; otherwise (after the wait, behind
+    // the staging of a and the first step's loads: issued ahead of the
+    // staging it delayed a and measured 2-4 % slower) only when the CTA
+    // streams more than one row tile (4096 x 4096, a single tile per CTA,
+    // measured 6 % slower with it).
     // Lane r issues row r's.  A slice of one step prefetches nothing
     // (asking for the first step of the next tile's rows instead measured
     // 2-4 % slower at k = 1000).
@@ -265,8 +272,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
     }
   }
   for (int m = 1; m <= pf; ++m) prefetch_tile(m);
-  // a is staged before the wait only when the caller promised that the
-  // predecessor does not write it (kFlagPrefetchA); c is always written
+  // With B promised, a is staged here: before the wait only when the
+  // caller promised that the predecessor does not write it either
+  // (kFlagPrefetchA), else after it.  c is always written
   // after the wait.  With kFlagDeferStores (only set with kFlagPrefetchA)
   // the CTA's row results are kept in shared memory and written after a
   // single wait at the end: the whole stream of B then overlaps the
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) gemv_tiles_kernel(Params p) {
   const bool defer = early_a && (p.flags & kFlagDeferStores) != 0;
   float *res = ps + 2 * W * R;  // [nloc] row results when deferring
   if (early && !early_a) wait_for_predecessor();
-  stage_a_shifted(p, as4, j0, len, off);
+  if (early) stage_a_shifted(p, as4, j0, len, off);
   __syncthreads();
   if (early_a && !defer) wait_for_predecessor();
 
