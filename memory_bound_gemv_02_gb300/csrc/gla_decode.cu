@@ -326,7 +326,13 @@ __global__ void __launch_bounds__(kGlaThreads, 3) gla_decode_kernel_small(GlaPar
 // too where the two choose the same G (G sets the row blocks o is summed in).
 // Before waiting on the preceding kernel, warp 0 asks L2 for the first
 // round's state (or, with GLA_PREFETCH_STATE, every thread already copies
-// its part of it): measured 3-8 % faster back to back.
+// its part of it): measured 3-8 % faster back to back.  A round's q, k, gk
+// and v are copied before its state (the whole round waits for both, and
+// the small rows no longer queue behind the state's chunks): 4096 x 64 x
+// 64 fp16 12.60 -> 12.21 us back to back, 16384 x 16 x 64 15.41 -> 15.02,
+// 2048 x 128 x 128 bf16 21.95 -> 21.79, 4096 x 128 x 128 bf16 42.04 ->
+// 42.23.  (Loading the CTA layout's first q, k, gk values ahead of its
+// state rows instead measured up to 12 % slower there.)
 constexpr int kGlaPipeRoundChunks = 2048;
 constexpr int64_t kGlaPairPackMaxHead = 16 * 1024;  // state bytes of a head up to which S_new is stored through pack_pairs
 // Shared memory of one CTA at most: two CTAs per SM (228 KB, 1 KB reserved
@@ -423,15 +429,16 @@ __global__ void __launch_bounds__(kGlaThreads) gla_decode_pipe_kernel(GlaParams 
   } else {
     if (t < 32) prefetch_first_round(p, ES, r, G);
     wait_for_predecessor();
+    issue_vectors(r, 0);
     issue_state(r, 0);
   }
-  issue_vectors(r, 0);
+  if (p.early_state) issue_vectors(r, 0);
   cp_async_commit();
   for (int b = 0; r < rounds; r += gridDim.x, b ^= 1) {
     const int64_t rn = r + gridDim.x;
     if (rn < rounds) {  // buffer b ^ 1 was last read before the previous round's second barrier
-      issue_state(rn, b ^ 1);
       issue_vectors(rn, b ^ 1);
+      issue_state(rn, b ^ 1);
     }
     cp_async_commit();
     cp_async_wait_all_but_one();  // this thread's copies of round r have landed
