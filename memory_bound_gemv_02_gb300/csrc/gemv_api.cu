@@ -37,7 +37,6 @@ constexpr int64_t kMaxSegments = 65536;         // most k-segments of any plan: 
 constexpr int kAutoVariant = GEMV_VARIANT_TILES;  // the planner's default family
 constexpr int kDefaultL2Prefetch = 0;              // tile rounds of L2 prefetch by default
 constexpr int kBulkDefaultStages = 2;              // ring buffers per warp of the bulk variant
-constexpr int64_t kBulkAutoBytes = 768LL << 20;    // B bytes from which the planner picks the bulk variant
 constexpr int kMaxSmemPerCta = 232448;  // 227 KiB, sm_100-family opt-in limit
 constexpr int64_t kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int64_t kSmemReservedPerCta = 1024;
@@ -435,22 +434,13 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
   const int auto_variant = (kAutoVariant == GEMV_VARIANT_ROWS && !aligned) ? GEMV_VARIANT_ROWS_GENERAL
                                                                             : kAutoVariant;
   const int variant = f->variant ? f->variant : auto_variant;
-  if (variant == GEMV_VARIANT_TILES && f == &fz) {
-    // Nothing forced: the tiles plan, or the bulk variant where it measured
-    // faster on GB300 than the tiles plan: B of 768 MiB or more whose rows
-    // the tiles plan streams with at most one warp each, i.e. a warp split
-    // no larger than its rows per warp (rows of at most ~1024 blocks;
-    // 57344 x 7168: 116.5 -> 114.5 us, 65536 x 7169: 135.3 -> 134.5 us back
-    // to back).  Below that, and for longer rows, register streaming is as
-    // fast or faster.
-    int st = plan_tiles(n, k, aligned, sm, f, out);
-    const int64_t b_bytes = n * k * 2;
-    if (st == GEMV_OK && out->warp_split <= out->rows_per_warp && b_bytes >= kBulkAutoBytes) {
-      gemv_config b{};
-      if (plan_tiles(n, k, aligned, sm, f, &b, true) == GEMV_OK) *out = b;
-    }
-    return st;
-  }
+  // Nothing forced: the tiles plan.  The bulk variant (forced only) was the
+  // planner's choice for B of 768 MiB or more with rows of at most ~1024
+  // blocks until the tiles kernel staged a ahead of its first B loads; as
+  // gemv() launches them it then measured faster or equal on 12 of 16 such
+  // shapes (131072 x 4096 151.6 -> 145.5 us, 262144 x 2048 150.2 -> 145.1,
+  // 65536 x 7169 134.2 -> 132.9, 57344 x 7168 113.0 -> 113.0) and slower on
+  // four by 0.6-1.6 % (98304 x 7168 190.1 -> 193.2).
   if (variant == GEMV_VARIANT_TILES) return plan_tiles(n, k, aligned, sm, f, out);
   if (variant == GEMV_VARIANT_BULK) return plan_tiles(n, k, aligned, sm, f, out, true);
   if (f->stages) return GEMV_ERR_CONFIG;
