@@ -31,6 +31,9 @@ static __device__ uint32_t g_gemv_wait_timeouts;
 namespace gemvk {
 namespace {
 
+constexpr int64_t kBulkAutoBytes = 768LL << 20;  // the planner's bulk variant: B bytes from which,
+constexpr int64_t kBulkAutoMinK = 6144;           // and the row lengths [kBulkAutoMinK, kBulkAutoEndK)
+constexpr int64_t kBulkAutoEndK = 8192;           // for which it is chosen
 constexpr int64_t kMaxSegment = 32768;  // columns of a staged per CTA (64 KiB of shared memory)
 constexpr int kMaxGridSplit = 64;              // most k-segments the planner adds to fill the GPU
 constexpr int64_t kMaxSegments = 65536;         // most k-segments of any plan: k <= INT32_MAX in 32768-column segments
@@ -434,13 +437,26 @@ int plan_impl(int64_t n, int64_t k, int dtype, bool aligned, int sm, const gemv_
   const int auto_variant = (kAutoVariant == GEMV_VARIANT_ROWS && !aligned) ? GEMV_VARIANT_ROWS_GENERAL
                                                                             : kAutoVariant;
   const int variant = f->variant ? f->variant : auto_variant;
-  // Nothing forced: the tiles plan.  The bulk variant (forced only) was the
-  // planner's choice for B of 768 MiB or more with rows of at most ~1024
-  // blocks until the tiles kernel staged a ahead of its first B loads; as
-  // gemv() launches them it then measured faster or equal on 12 of 16 such
-  // shapes (131072 x 4096 151.6 -> 145.5 us, 262144 x 2048 150.2 -> 145.1,
-  // 65536 x 7169 134.2 -> 132.9, 57344 x 7168 113.0 -> 113.0) and slower on
-  // four by 0.6-1.6 % (98304 x 7168 190.1 -> 193.2).
+  if (variant == GEMV_VARIANT_TILES && f == &fz) {
+    // Nothing forced: the tiles plan, or the bulk variant where it measured
+    // at least as fast on GB300: B of 768 MiB or more whose tiles plan
+    // streams each row with one warp, with rows of 6144 to 8191 elements.
+    // There (57344 x 7168, 65536 x 7169) the two are equal back to back as
+    // gemv() launches them, and the bulk kernel is 1-2 % faster as plain
+    // and as isolated launches (65536 x 7169 under ncu: 85.1 % of the DRAM
+    // peak against 80.8 %).  With shorter rows the tiles kernel, which
+    // stages a ahead of its first loads, is 2-4 % faster back to back
+    // (131072 x 4096 151.6 -> 145.5 us, 262144 x 2048 150.2 -> 145.1), and
+    // at k = 8192 on three of four shapes (57344 x 8192 130.2 -> 127.1).
+    int st = plan_tiles(n, k, aligned, sm, f, out);
+    const int64_t b_bytes = n * k * 2;
+    if (st == GEMV_OK && out->warp_split <= out->rows_per_warp && b_bytes >= kBulkAutoBytes &&
+        k >= kBulkAutoMinK && k < kBulkAutoEndK) {
+      gemv_config b{};
+      if (plan_tiles(n, k, aligned, sm, f, &b, true) == GEMV_OK) *out = b;
+    }
+    return st;
+  }
   if (variant == GEMV_VARIANT_TILES) return plan_tiles(n, k, aligned, sm, f, out);
   if (variant == GEMV_VARIANT_BULK) return plan_tiles(n, k, aligned, sm, f, out, true);
   if (f->stages) return GEMV_ERR_CONFIG;

@@ -2,8 +2,9 @@
 in the launch configuration gemv() picks (the one the benchmark times), one
 seed each, against the oracle; and, with integer-valued inputs (every fp32
 partial sum exact, so any summation order gives the same fp32 total), the
-automatic plans of the largest shapes, an unaligned tiles plan and the bulk
-kernel's plans of the large shapes bit for bit.
+automatic plans of the largest shapes (the bulk kernel's) and an unaligned
+tiles plan bit for bit, and the tiles kernel forced on the shapes the bulk
+kernel serves.
 
 The oracle runs over row chunks on a pool of host threads (rows are
 independent; each chunk is one unchanged oracle call).
@@ -41,7 +42,7 @@ def test_every_row_at_full_size(cuda_dev, n, k, dtype, out_fp32, dist):
 
 
 # (n, k, dtype, the variant gemv() is expected to pick)
-EXACT = [(57344, 7168, "f16", g.GEMV_VARIANT_TILES), (65536, 7169, "bf16", g.GEMV_VARIANT_TILES),
+EXACT = [(57344, 7168, "f16", g.GEMV_VARIANT_BULK), (65536, 7169, "bf16", g.GEMV_VARIANT_BULK),
          (18433, 7169, "f16", g.GEMV_VARIANT_TILES), (18433, 16384, "bf16", g.GEMV_VARIANT_TILES)]
 
 
@@ -58,14 +59,15 @@ def test_automatic_plans_bit_exact_at_full_size(cuda_dev, n, k, dtype, variant):
 
 
 @pytest.mark.parametrize("n,k,dtype", [(57344, 7168, "f16"), (65536, 7169, "bf16")])
-def test_bulk_plans_bit_exact_at_full_size(cuda_dev, n, k, dtype):
-    """The bulk kernel (forced) on the large shapes, its own plan, every
-    row bit for bit with integer-valued inputs."""
+def test_forced_tiles_plans_bit_exact_at_full_size(cuda_dev, n, k, dtype):
+    """The tiles kernel (forced) on the large shapes the bulk kernel serves
+    by default, its own plan, every row bit for bit with integer-valued
+    inputs."""
     B, a = inputs.make_int_inputs(n, k, dtype, seed=n + k + 1, device=cuda_dev)
     for out_fp32 in (False, True):
-        c = g.gemv_ex(B, a, out_fp32=out_fp32, config={"variant": g.GEMV_VARIANT_BULK})
+        c = g.gemv_ex(B, a, out_fp32=out_fp32, config={"variant": g.GEMV_VARIANT_TILES})
         used = g.gemv_last_config()
-        assert used["variant"] == g.GEMV_VARIANT_BULK, used
+        assert used["variant"] == g.GEMV_VARIANT_TILES, used
         assert exact_bits_match(c, B, a, out_fp32), (n, k, dtype, out_fp32, used)
         del c
         torch.cuda.empty_cache()

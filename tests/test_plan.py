@@ -393,16 +393,28 @@ def test_bulk_invalid_configs_rejected(gemv_lib, cfg):
 
 
 @pytest.mark.parametrize("aligned", [True, False])
-def test_auto_choice_is_tiles(gemv_lib, aligned):
-    """Unforced plans are the tiles plan on every shape, including the
-    large ones the bulk variant once served; the bulk variant is forced
-    only."""
-    for n, k in WORKLOADS + [(65536, 7169), (16384, 7169), (18432, 7168), (65536, 16384), (131072, 4096),
-                             (98304, 7168), (262144, 2048)]:
+def test_bulk_auto_choice(gemv_lib, aligned):
+    """Unforced plans use the bulk variant (with its own plan) exactly for B
+    of at least 768 MiB whose tiles plan has one warp per row and whose rows
+    hold 6144 to 8191 elements; everything else is the tiles plan."""
+    shapes = WORKLOADS + [(65536, 7169), (16384, 7169), (18432, 7168), (65536, 16384), (131072, 4096),
+                          (98304, 7168), (262144, 2048), (57344, 8192), (65536, 8192), (131072, 6144),
+                          (131072, 6143)]
+    for n, k in shapes:
         auto = gemv_lib.gemv_plan(n, k, 0, aligned, SM)
         tiles = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 3})
-        assert auto == tiles and auto["variant"] == 3, (n, k, aligned)
-    assert gemv_lib.gemv_plan(57344, 7168, 1, True, SM, config={"variant": 4})["variant"] == 4
+        if n * k * 2 >= (768 << 20) and tiles["warp_split"] <= tiles["rows_per_warp"] and 6144 <= k < 8192:
+            assert auto["variant"] == 4, (n, k, aligned)
+            assert auto == gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 4})
+        else:
+            assert auto == tiles and auto["variant"] == 3, (n, k, aligned)
+    assert gemv_lib.gemv_plan(57344, 7168, 1, True, SM)["variant"] == 4
+    assert gemv_lib.gemv_plan(65536, 7169, 0, False, SM)["variant"] == 4
+    assert gemv_lib.gemv_plan(131072, 4096, 0, True, SM)["variant"] == 3
+    assert gemv_lib.gemv_plan(57344, 8192, 0, True, SM)["variant"] == 3
+    assert gemv_lib.gemv_plan(16384, 7169, 0, False, SM)["variant"] == 3
+    assert gemv_lib.gemv_plan(7168, 16384, 0, True, SM)["variant"] == 3
+    assert gemv_lib.gemv_plan(18432, 7168, 1, True, SM)["variant"] == 3
 
 
 @pytest.mark.parametrize("n,k,base_off", [(16384, 7169, 0)])
