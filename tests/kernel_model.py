@@ -420,6 +420,28 @@ def gla_partial_store_conflicts(cpr, vec, dv):
     return extra
 
 
+def gla_store_o_schedule(nh, G, dv, RP, nthreads=256):
+    """Replay of the GLA step's o epilogue (``store_o``, four outputs per
+    thread): thread t takes outputs x = 4 * x4 .. 4 * x4 + 3 for x4 = t,
+    t + nthreads, ... < nh * dv / 4, reading the 16-byte partials at float
+    offset (g * RP + rb) * dv + j (x = g * dv + j) for rb < RP.  Checks that
+    every output of the round is written once, that the four outputs of a
+    thread belong to one head (j % 4 == 0, dv % 4 == 0), and that every
+    partial read is 16-byte aligned and inside part[G][RP][dv]."""
+    assert dv % 4 == 0 and nh <= G
+    writes = np.zeros(nh * dv, dtype=np.int64)
+    for t in range(nthreads):
+        for x4 in range(t, nh * dv // 4, nthreads):
+            x = 4 * x4
+            g, j = divmod(x, dv)
+            assert j + 3 < dv and g < nh
+            for rb in range(RP):
+                off = (g * RP + rb) * dv + j
+                assert off % 4 == 0 and 0 <= off and off + 4 <= G * RP * dv
+            writes[x:x + 4] += 1
+    assert (writes == 1).all()
+
+
 def gla_balanced_grid(units, cap):
     """The host's grid for `units` rounds dealt round-robin over at most
     `cap` resident CTAs: the fewest rounds per CTA, then the fewest CTAs --

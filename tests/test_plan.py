@@ -517,3 +517,15 @@ def test_ragged_tail_plans_replay(gemv_lib, variant):
         p = gemv_lib.gemv_plan(n, k, 0, True, SM, config=cfg)
         if n * k <= 300000:
             kernel_model.replay(n, k, p)
+
+
+@pytest.mark.parametrize("G,dk,dv", [(1, 128, 128), (4, 64, 64), (16, 16, 64), (2, 256, 256), (8, 32, 32),
+                                     (1, 64, 8), (32, 8, 8), (3, 64, 64)])
+@pytest.mark.parametrize("partial", [False, True])
+def test_gla_store_o_schedule(G, dk, dv, partial):
+    """The GLA step's vectorised o epilogue writes each output of a round
+    once and reads only its heads' partials, for full and short last rounds."""
+    cpr = dv // 8
+    RP = max(1, (256 // G) // cpr)
+    nh = max(1, G - 1) if partial else G
+    kernel_model.gla_store_o_schedule(nh, G, dv, RP)
