@@ -112,9 +112,10 @@ enum {
                                  while the preceding kernel drains; it waits for that
                                  kernel's completion (and its memory) before reading or
                                  writing any global memory.  Before the wait it only asks L2
-                                 to prefetch its first tile of B (and, right after it, the
-                                 second step of its rows): hints, which read nothing into
-                                 the kernel and need no promise */
+                                 to prefetch its first tile of B: a hint, which reads
+                                 nothing into the kernel and needs no promise.  After it,
+                                 a is staged first, then the first tile of B is loaded and
+                                 L2 is asked for the second step of its rows */
   /* "Work still running on the stream", for the two promises below: every
      kernel launched on the stream after its last ordinary operation (a kernel
      launched without the programmatic-serialization attribute, a copy, a memset
@@ -127,7 +128,11 @@ enum {
                                  waiting.  The caller guarantees
                                  that no work still running on the stream writes B (true
                                  for weights); a and c are still accessed only after the
-                                 wait */
+                                 wait, so a is staged behind those loads.  Measured on
+                                 GB300 it is slower than GEMV_OVERLAP_PDL on most shapes
+                                 whose CTAs stream several row tiles (7168 x 16384 fp16:
+                                 33.2 against 31.8 us per call back to back) and faster
+                                 on a few small or bulk-variant ones */
   GEMV_OVERLAP_PDL_PREFETCH_BA = 3 /* as GEMV_OVERLAP_PDL_PREFETCH_B, and a is also read
                                  (staged) before waiting: the caller guarantees that no work
                                  still running on the stream writes B or a -- e.g. several
