@@ -63,9 +63,6 @@ struct GlaIo<F16> {
     for (int q = 0; q < 4; ++q) w[q] = (uint32_t)F16::from_float(f[2 * q]) | ((uint32_t)F16::from_float(f[2 * q + 1]) << 16);
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
-  static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
-    static_cast<uint16_t *>(p)[i] = F16::from_float(x);
-  }
   // As pack(), rounding each pair with one paired conversion (the same
   // nearest-even rounding of each element, hence the same bits).
   static __device__ __forceinline__ uint4 pack_pairs(const float (&f)[VEC]) {
@@ -78,7 +75,6 @@ struct GlaIo<F16> {
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
   // Elements i .. i + 3 (i % 4 == 0, p 8-byte aligned), by paired conversions.
-  static constexpr int kStore4Align = 8;
   static __device__ __forceinline__ void store4(void *p, int64_t i, float a, float b, float c, float d) {
     const __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
     static_cast<uint2 *>(p)[i >> 2] =
@@ -100,9 +96,6 @@ struct GlaIo<BF16> {
       w[q] = (uint32_t)BF16::from_float(f[2 * q]) | ((uint32_t)BF16::from_float(f[2 * q + 1]) << 16);
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
-  static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
-    static_cast<uint16_t *>(p)[i] = BF16::from_float(x);
-  }
   static __device__ __forceinline__ uint4 pack_pairs(const float (&f)[VEC]) {
     uint32_t w[4];
 #pragma unroll
@@ -112,7 +105,6 @@ struct GlaIo<BF16> {
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
-  static constexpr int kStore4Align = 8;
   static __device__ __forceinline__ void store4(void *p, int64_t i, float a, float b, float c, float d) {
     const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
     static_cast<uint2 *>(p)[i >> 2] =
@@ -132,11 +124,7 @@ struct GlaIo<F32> {
   static __device__ __forceinline__ uint4 pack(const float (&f)[VEC]) {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
   }
-  static __device__ __forceinline__ void store_scalar(void *p, int64_t i, float x) {
-    static_cast<float *>(p)[i] = x;
-  }
   static __device__ __forceinline__ uint4 pack_pairs(const float (&f)[VEC]) { return pack(f); }
-  static constexpr int kStore4Align = 16;
   static __device__ __forceinline__ void store4(void *p, int64_t i, float a, float b, float c, float d) {
     static_cast<float4 *>(p)[i >> 2] = make_float4(a, b, c, d);
   }
@@ -165,37 +153,29 @@ __device__ __forceinline__ void stg_stream(uint4 *p, const uint4 &v) {
 
 // o of a round of nh heads from the row-block partials part[G][RP][dv]:
 // o[h0 * dv + x] = scale * (0 + part[g][0][j] + part[g][1][j] + ...), x =
-// g * dv + j, the row blocks added in ascending order.  With o aligned for
-// it, each thread takes four consecutive outputs (one 16-byte read of the
-// partials per row block, one store of the four results through paired
-// conversions: the same rounding, hence the same bits as one at a time);
-// at 16384 x 16 x 64 fp16 a round has 1024 outputs, and storing them one at
-// a time took 21 % more instructions than a 64 x 64 step of the same bytes.
+// g * dv + j, the row blocks added in ascending order.  Each thread takes
+// four consecutive outputs (one 16-byte read of the partials per row block,
+// one store of the four results through paired conversions: the same
+// rounding, hence the same bits as one at a time); o is 16-byte aligned (the
+// host checks it) and dv % 4 == 0, so each store is aligned.  At 16384 x 16
+// x 64 fp16 a round has 1024 outputs, and storing them one at a time took
+// 21 % more instructions than a 64 x 64 step of the same bytes.
 template <class T>
 __device__ __forceinline__ void store_o(const GlaParams &p, const float *part, int64_t h0, int nh, int dv, int RP,
                                         int t, int nthreads) {
   using IO = GlaIo<T>;
-  if ((reinterpret_cast<uintptr_t>(p.o) & (uintptr_t)(IO::kStore4Align - 1)) == 0) {
-    const int n4 = nh * dv / 4;  // dv % 4 == 0 (dv % VEC == 0)
-    for (int x4 = t; x4 < n4; x4 += nthreads) {
-      const int x = 4 * x4, g = x / dv, j = x % dv;
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      for (int rb = 0; rb < RP; ++rb) {
-        const float4 v = *reinterpret_cast<const float4 *>(part + (g * RP + rb) * dv + j);
-        s0 += v.x;
-        s1 += v.y;
-        s2 += v.z;
-        s3 += v.w;
-      }
-      IO::store4(p.o, h0 * dv + x, p.scale * s0, p.scale * s1, p.scale * s2, p.scale * s3);
+  const int n4 = nh * dv / 4;  // dv % 4 == 0 (dv % VEC == 0)
+  for (int x4 = t; x4 < n4; x4 += nthreads) {
+    const int x = 4 * x4, g = x / dv, j = x % dv;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int rb = 0; rb < RP; ++rb) {
+      const float4 v = *reinterpret_cast<const float4 *>(part + (g * RP + rb) * dv + j);
+      s0 += v.x;
+      s1 += v.y;
+      s2 += v.z;
+      s3 += v.w;
     }
-  } else {
-    for (int x = t; x < nh * dv; x += nthreads) {
-      const int g = x / dv, j = x % dv;
-      float sum = 0.f;
-      for (int rb = 0; rb < RP; ++rb) sum += part[(g * RP + rb) * dv + j];
-      IO::store_scalar(p.o, h0 * dv + x, p.scale * sum);
-    }
+    IO::store4(p.o, h0 * dv + x, p.scale * s0, p.scale * s1, p.scale * s2, p.scale * s3);
   }
 }
 
