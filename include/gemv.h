@@ -100,8 +100,8 @@ enum {
                                     sm_103a form of the multi-stage shared-memory pipeline of
                                     B (TileLang Case Studies, Case B.1 "O3 Pipelined B
                                     Loads").  The planner picks it for B of 768 MiB or more
-                                    when the tiles plan has one warp per row (rows of at
-                                    most 1024 16-byte blocks); otherwise only when forced */
+                                    when the tiles plan has one warp per row and the rows
+                                    hold 6144 to 8191 elements; otherwise only when forced */
 };
 
 /* Launch overlap with the preceding work on the stream (gemv_config.overlap). */

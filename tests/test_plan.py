@@ -399,7 +399,7 @@ def test_bulk_auto_choice(gemv_lib, aligned):
     hold 6144 to 8191 elements; everything else is the tiles plan."""
     shapes = WORKLOADS + [(65536, 7169), (16384, 7169), (18432, 7168), (65536, 16384), (131072, 4096),
                           (98304, 7168), (262144, 2048), (57344, 8192), (65536, 8192), (131072, 6144),
-                          (131072, 6143)]
+                          (131072, 6143), (98304, 8191), (98304, 8192), (49152, 8000)]
     for n, k in shapes:
         auto = gemv_lib.gemv_plan(n, k, 0, aligned, SM)
         tiles = gemv_lib.gemv_plan(n, k, 0, aligned, SM, config={"variant": 3})
